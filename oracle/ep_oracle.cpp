@@ -1,0 +1,348 @@
+// Oracle for MoE token layout, dispatch and combine: TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, single-threaded CPU restatement of what the hot path
+// computes. It is used by the tests, by the package's smoke check and by the
+// benchmark's CPU baseline; nothing in the product path may call it. It shares
+// no code, header, table or helper with the CUDA library: every encoder below
+// is written from the format's definition.
+//
+// Sources (the DeepEP write-ups this project follows):
+//  * "DeepEP Ascend deep dive" (kongchang.com), section "Two Transfers:
+//    Dispatch and Combine": a token reaches a card once even when several of
+//    its experts live there; combine weights each expert output by the router
+//    score and sums. Section "Dispatch's Three Phases": tokens are cloned once
+//    per chosen expert and reordered by expert (the "expand" layout); the
+//    volume example 16,384 x 7,168 x 2 B x 6 copies.
+//  * "DeepEP lesson 14" (hpc.payai.win), section "practice task": dispatch
+//    appends (i, x_i) to expert e's queue for every (i, k) in order; combine
+//    adds w_ik * f_e(x_i) for every k.
+//  * "DeepEP V1 (legacy) guide" (zskr.cn), section 5.2(1): the layout returns
+//    num_tokens_per_rank, num_tokens_per_expert and the is_token_in_rank mask;
+//    section 5.2(6): FP8 data with float scales of shape [tokens, hidden/128];
+//    section 6.1/6.3: low-latency receive buffer
+//    [num_local_experts, num_ranks * max_tokens, hidden] plus per-expert
+//    receive counts; -1 in topk_idx is a legal "no expert".
+//
+// Readings where the pages leave a step open (each one is listed with its
+// reason in the design notes of this repository):
+//  * expert e lives on rank e / (E / R) (contiguous blocks of experts);
+//  * slots are assigned in (token, top-k) order: global token order is
+//    source-rank-then-token order when tokens are split contiguously;
+//  * an index outside [-1, E) is treated as masked and raises EP_BAD_INDEX;
+//  * FP8: s = amax / 448 in fp32 (round to nearest), q = e4m3(x / s) with an
+//    IEEE fp32 division, round to nearest even, saturating to +-448; an
+//    all-zero block has s = 0 and q = e4m3(x) (signed zeros);
+//  * combine: acc = +0, then acc = fmaf(w_k, y_k, acc) for k ascending over
+//    unmasked slots, output BF16 rounded to nearest even.
+//
+// Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -shared -fPIC.
+// The only fused multiply-add is the explicit std::fmaf of the combine.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <utility>
+#include <vector>
+
+namespace {
+
+// Data-dependent conditions, reported as bits of the returned status.
+constexpr int kBadIndex = 1;   // an index outside [-1, E)
+constexpr int kCapacity = 2;   // a destination row beyond the given capacity
+constexpr int kLLOverflow = 4; // more than T tokens from one source rank
+
+// ---------------------------------------------------------------- BF16 ----
+// BF16 is the upper half of an IEEE binary32 word. Rounding to nearest even
+// looks at the discarded lower half: above the midpoint rounds up, at the
+// midpoint rounds to the even upper half. NaN stays NaN (made quiet).
+uint16_t bf16_from_f32(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  const bool is_nan = (u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0;
+  if (is_nan) return static_cast<uint16_t>((u >> 16) | 0x0040u);
+  uint32_t upper = u >> 16;
+  const uint32_t lower = u & 0xFFFFu;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;
+  return static_cast<uint16_t>(upper);
+}
+
+float f32_from_bf16(uint16_t h) {
+  const uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// ---------------------------------------------------------------- E4M3 ----
+// OCP 8-bit floating point, E4M3 ("fn": finite, no infinities): 1 sign bit,
+// 4 exponent bits with bias 7, 3 mantissa bits. Exponent field 0 holds
+// subnormals m * 2^-9; fields 1..15 hold (1 + m/8) * 2^(field - 7), except
+// field 15 with m = 7, which is NaN. The largest finite value is 448.
+
+double round_half_even(double y) {
+  const double f = std::floor(y);
+  const double d = y - f;
+  if (d > 0.5) return f + 1.0;
+  if (d < 0.5) return f;
+  return std::fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+uint8_t e4m3_from_f32(float v) {
+  if (std::isnan(v)) return 0x7F;
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  const double a = std::fabs(static_cast<double>(v));
+  if (a >= 448.0) return sign | 0x7E;  // saturate to the largest finite value
+  if (a < 0.015625) {                  // below 2^-6: quantum 2^-9
+    const double n = round_half_even(a * 512.0);  // 0..8; 8 is the code of 2^-6
+    return sign | static_cast<uint8_t>(n);
+  }
+  int e2;
+  std::frexp(a, &e2);          // a = m * 2^e2 with m in [0.5, 1)
+  const int ex = e2 - 1;       // floor(log2 a), in [-6, 8]
+  const double quantum = std::ldexp(1.0, ex - 3);
+  const double n = round_half_even(a / quantum);  // 8..16, exact division
+  int code = ((ex + 7) << 3) + static_cast<int>(n) - 8;  // n == 16 carries
+  if (code > 0x7E) code = 0x7E;
+  return sign | static_cast<uint8_t>(code);
+}
+
+double e4m3_to_f64(uint8_t c) {
+  const double s = (c & 0x80) ? -1.0 : 1.0;
+  const int field = (c >> 3) & 0xF;
+  const int m = c & 0x7;
+  if (field == 15 && m == 7) return std::nan("");
+  if (field == 0) return s * std::ldexp(static_cast<double>(m), -9);
+  return s * std::ldexp(1.0 + m / 8.0, field - 7);
+}
+
+// Per 128-channel block b of one BF16 row: amax_b = max |x|, s_b = amax_b / 448
+// (fp32, round to nearest), q = e4m3(x / s_b).
+void quantize_row(const uint16_t* x, int H, uint8_t* q, float* scales) {
+  for (int b = 0; b < H / 128; ++b) {
+    float amax = 0.0f;
+    for (int i = 0; i < 128; ++i) {
+      const float a = std::fabs(f32_from_bf16(x[b * 128 + i]));
+      if (a > amax) amax = a;
+    }
+    const float s = amax / 448.0f;
+    scales[b] = s;
+    for (int i = 0; i < 128; ++i) {
+      const float xi = f32_from_bf16(x[b * 128 + i]);
+      q[b * 128 + i] = (s > 0.0f) ? e4m3_from_f32(xi / s) : e4m3_from_f32(xi);
+    }
+  }
+}
+
+bool valid_expert(int32_t e, int E) { return e >= 0 && e < E; }
+
+// Copy (or quantise) token t's row into destination row `row` of a receive
+// buffer. `payload` is the token's row already encoded (BF16 or E4M3).
+void write_row(const uint8_t* payload, const float* scales, int H, int use_fp8,
+               void* dst_x, float* dst_scales, int64_t row) {
+  const size_t row_bytes = static_cast<size_t>(H) * (use_fp8 ? 1 : 2);
+  std::memcpy(static_cast<uint8_t*>(dst_x) + row * row_bytes, payload, row_bytes);
+  if (use_fp8 && dst_scales)
+    std::memcpy(dst_scales + row * (H / 128), scales, sizeof(float) * (H / 128));
+}
+
+}  // namespace
+
+extern "C" {
+
+uint16_t oracle_bf16_from_f32(float f) { return bf16_from_f32(f); }
+uint8_t oracle_e4m3_from_f32(float f) { return e4m3_from_f32(f); }
+double oracle_e4m3_to_f64(uint8_t c) { return e4m3_to_f64(c); }
+
+void oracle_bf16_from_f32_n(const float* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = bf16_from_f32(in[i]);
+}
+
+void oracle_e4m3_from_f32_n(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_from_f32(in[i]);
+}
+
+// rows x H BF16 -> rows x H E4M3 and rows x H/128 fp32 scales.
+void oracle_quantize_rows(const uint16_t* x, int64_t rows, int H, uint8_t* q, float* scales) {
+  for (int64_t r = 0; r < rows; ++r)
+    quantize_row(x + r * H, H, q + r * H, scales + r * (H / 128));
+}
+
+// Routing layout.
+//   per_expert[e]  = #{(t,k) : idx[t,k] == e}
+//   mask[t,r]      = 1 if some k has a valid idx[t,k] on rank r (one copy per rank)
+//   per_rank[r]    = sum_t mask[t,r]
+//   expert_off, rank_off: exclusive prefix sums, length E+1 and R+1
+//   expert_slot[t,k] = expert_off[e] + position of (t,k) in expert e's list
+//   rank_slot[t,r]   = rank_off[r] + position of t in rank r's list
+// Lists are built by visiting (t, k) in order, so they are in token order.
+int oracle_layout(const int32_t* idx, int N, int K, int E, int R,
+                  int32_t* per_rank, int32_t* per_expert, uint8_t* mask,
+                  int32_t* rank_off, int32_t* expert_off,
+                  int32_t* rank_slot, int32_t* expert_slot) {
+  int status = 0;
+  const int L = E / R;
+  std::vector<std::vector<std::pair<int, int>>> expert_list(E);
+  std::vector<std::vector<int>> rank_list(R);
+  std::vector<char> seen(R);
+  for (int t = 0; t < N; ++t) {
+    std::fill(seen.begin(), seen.end(), 0);
+    for (int k = 0; k < K; ++k) {
+      const int32_t e = idx[static_cast<int64_t>(t) * K + k];
+      if (e == -1) continue;
+      if (!valid_expert(e, E)) { status |= kBadIndex; continue; }
+      expert_list[e].push_back({t, k});
+      const int r = e / L;
+      if (!seen[r]) { seen[r] = 1; rank_list[r].push_back(t); }
+    }
+  }
+  expert_off[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    per_expert[e] = static_cast<int32_t>(expert_list[e].size());
+    expert_off[e + 1] = expert_off[e] + per_expert[e];
+  }
+  rank_off[0] = 0;
+  for (int r = 0; r < R; ++r) {
+    per_rank[r] = static_cast<int32_t>(rank_list[r].size());
+    rank_off[r + 1] = rank_off[r] + per_rank[r];
+  }
+  for (int64_t i = 0; i < static_cast<int64_t>(N) * K; ++i) expert_slot[i] = -1;
+  for (int64_t i = 0; i < static_cast<int64_t>(N) * R; ++i) { rank_slot[i] = -1; mask[i] = 0; }
+  for (int e = 0; e < E; ++e)
+    for (size_t j = 0; j < expert_list[e].size(); ++j) {
+      const auto [t, k] = expert_list[e][j];
+      expert_slot[static_cast<int64_t>(t) * K + k] = expert_off[e] + static_cast<int32_t>(j);
+    }
+  for (int r = 0; r < R; ++r)
+    for (size_t j = 0; j < rank_list[r].size(); ++j) {
+      const int t = rank_list[r][j];
+      rank_slot[static_cast<int64_t>(t) * R + r] = rank_off[r] + static_cast<int32_t>(j);
+      mask[static_cast<int64_t>(t) * R + r] = 1;
+    }
+  return status;
+}
+
+// Dispatch: every token row goes once to each rank in its mask (per-rank
+// receive buffer, rows packed by rank_off) and once per unmasked top-k slot to
+// the expert-major buffer (rows packed by expert_off). In FP8 mode the row is
+// quantised once and the same bytes and scales are written to every copy.
+// Per-rank metadata: src[row] = t; topk_idx[row,k] = local expert id if
+// expert k of t lives on that rank, else -1; topk_w[row,k] = w or 0.
+// Expert-major metadata: src[row] = t*K + k. Any output pointer may be null.
+int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
+                    int N, int K, int H, int E, int R, int use_fp8,
+                    const int32_t* rank_slot, const int32_t* expert_slot,
+                    void* rank_x, float* rank_scales, int32_t* rank_src,
+                    int32_t* rank_topk_idx, float* rank_topk_w, int64_t rank_cap,
+                    void* exp_x, float* exp_scales, int32_t* exp_src, int64_t exp_cap) {
+  int status = 0;
+  const int L = E / R;
+  std::vector<uint8_t> q(H);
+  std::vector<float> sc(H / 128 > 0 ? H / 128 : 1);
+  for (int t = 0; t < N; ++t) {
+    const uint16_t* xt = x + static_cast<int64_t>(t) * H;
+    const uint8_t* payload = reinterpret_cast<const uint8_t*>(xt);
+    if (use_fp8) {
+      quantize_row(xt, H, q.data(), sc.data());
+      payload = q.data();
+    }
+    for (int r = 0; r < R; ++r) {
+      const int32_t row = rank_slot[static_cast<int64_t>(t) * R + r];
+      if (row < 0) continue;
+      if (row >= rank_cap) { status |= kCapacity; continue; }
+      if (rank_x) write_row(payload, sc.data(), H, use_fp8, rank_x, rank_scales, row);
+      if (rank_src) rank_src[row] = t;
+      for (int k = 0; k < K; ++k) {
+        const int32_t e = idx[static_cast<int64_t>(t) * K + k];
+        const bool here = valid_expert(e, E) && e / L == r;
+        if (rank_topk_idx) rank_topk_idx[static_cast<int64_t>(row) * K + k] = here ? e - r * L : -1;
+        if (rank_topk_w) rank_topk_w[static_cast<int64_t>(row) * K + k] = here ? w[static_cast<int64_t>(t) * K + k] : 0.0f;
+      }
+    }
+    for (int k = 0; k < K; ++k) {
+      const int32_t row = expert_slot[static_cast<int64_t>(t) * K + k];
+      if (row < 0) continue;
+      if (row >= exp_cap) { status |= kCapacity; continue; }
+      if (exp_x) write_row(payload, sc.data(), H, use_fp8, exp_x, exp_scales, row);
+      if (exp_src) exp_src[row] = t * K + k;
+    }
+  }
+  return status;
+}
+
+// Combine: out[t] = bf16( sum over k ascending with slot[t,k] >= 0 of
+// w[t,k] * y[slot[t,k]] ), each term added with one fp32 fused multiply-add
+// onto an accumulator that starts at +0.
+int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const float* w,
+                   int N, int K, int H, uint16_t* out) {
+  int status = 0;
+  std::vector<float> acc(H);
+  for (int t = 0; t < N; ++t) {
+    std::fill(acc.begin(), acc.end(), 0.0f);
+    for (int k = 0; k < K; ++k) {
+      const int32_t row = slot[static_cast<int64_t>(t) * K + k];
+      if (row < 0) continue;
+      if (row >= y_rows) { status |= kCapacity; continue; }
+      const float wk = w[static_cast<int64_t>(t) * K + k];
+      const uint16_t* yr = y + static_cast<int64_t>(row) * H;
+      for (int h = 0; h < H; ++h) acc[h] = std::fmaf(wk, f32_from_bf16(yr[h]), acc[h]);
+    }
+    for (int h = 0; h < H; ++h) out[static_cast<int64_t>(t) * H + h] = bf16_from_f32(acc[h]);
+  }
+  return status;
+}
+
+// Low-latency dispatch. Tokens are split contiguously over R source ranks,
+// n_s = N / R each (n_s <= T). The receive buffer of expert e is the fixed
+// region [e][0 .. R*T) of recv_x [E, R*T, H]; the rank owning e sees it as
+// its local expert e - r*L, i.e. [L, R*T, H] per rank. Expert e's received
+// rows are packed at j = 0 .. count-1 in token order; rows at j >= count are
+// not written.
+//   recv_count[e]      = number of (t,k) routed to e
+//   recv_src[e, j]     = global token index of row j
+//   layout_range[e, s] = (offset << 32) | count for the rows from source s
+//   slot_map[t, k]     = e * R*T + j, or -1 if masked
+int oracle_ll_dispatch(const uint16_t* x, const int32_t* idx, int N, int K, int H,
+                       int E, int R, int T, int use_fp8,
+                       void* recv_x, float* recv_scales, int32_t* recv_src,
+                       int32_t* recv_count, int64_t* layout_range, int32_t* slot_map) {
+  int status = 0;
+  const int n_s = N / R;
+  if (n_s > T) status |= kLLOverflow;
+  const int64_t cap = static_cast<int64_t>(R) * T;
+  std::vector<std::vector<std::pair<int, int>>> expert_list(E);
+  for (int t = 0; t < N; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int32_t e = idx[static_cast<int64_t>(t) * K + k];
+      slot_map[static_cast<int64_t>(t) * K + k] = -1;
+      if (e == -1) continue;
+      if (!valid_expert(e, E)) { status |= kBadIndex; continue; }
+      expert_list[e].push_back({t, k});
+    }
+  std::vector<uint8_t> q(H);
+  std::vector<float> sc(H / 128 > 0 ? H / 128 : 1);
+  for (int e = 0; e < E; ++e) {
+    recv_count[e] = static_cast<int32_t>(expert_list[e].size());
+    std::vector<int64_t> count_from(R, 0);
+    for (size_t j = 0; j < expert_list[e].size(); ++j) {
+      const auto [t, k] = expert_list[e][j];
+      if (static_cast<int64_t>(j) >= cap) { status |= kLLOverflow; continue; }
+      const int64_t row = static_cast<int64_t>(e) * cap + static_cast<int64_t>(j);
+      const uint16_t* xt = x + static_cast<int64_t>(t) * H;
+      const uint8_t* payload = reinterpret_cast<const uint8_t*>(xt);
+      if (use_fp8) { quantize_row(xt, H, q.data(), sc.data()); payload = q.data(); }
+      write_row(payload, sc.data(), H, use_fp8, recv_x, recv_scales, row);
+      recv_src[row] = t;
+      slot_map[static_cast<int64_t>(t) * K + k] = static_cast<int32_t>(row);
+      const int s = (n_s > 0) ? t / n_s : 0;
+      if (s < R) count_from[s] += 1;
+    }
+    int64_t offset = 0;
+    for (int s = 0; s < R; ++s) {
+      layout_range[static_cast<int64_t>(e) * R + s] = (offset << 32) | count_from[s];
+      offset += count_from[s];
+    }
+  }
+  return status;
+}
+
+}  // extern "C"

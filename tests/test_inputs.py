@@ -1,0 +1,80 @@
+"""The seeded input generator: determinism, shapes and the routing recipes."""
+import numpy as np
+import pytest
+
+import epinputs as ei
+
+
+def test_splitmix64_known_sequence():
+    # SplitMix64 seeded with 0: the first outputs of the published generator
+    # (Vigna's reference implementation of Steele-Lea-Flood's SplitMix64).
+    got = ei.splitmix64(0, 3)
+    assert [int(v) for v in got] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_splitmix64_offsets_agree():
+    a = ei.splitmix64(12345, 1000)
+    b = ei.splitmix64(12345, 500, start=500)
+    assert np.array_equal(a[500:], b)
+
+
+def test_normal_moments():
+    z = ei.normal(ei.stream_key(0, 1), 1 << 20)
+    assert abs(z.mean()) < 5e-3
+    assert abs(z.std() - 1.0) < 5e-3
+
+
+def test_bf16_bits_roundtrip_nearest():
+    f = np.array([1.0, -2.5, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -9, 1.0 + 3 * 2 ** -8], np.float32)
+    b = ei.bf16_bits_from_f32(f)
+    # BF16 spacing at 1 is 2^-7. 1 + 2^-8 is a tie between 1 and 1 + 2^-7:
+    # the even mantissa wins (1.0). 1 + 3*2^-9 is past the midpoint (up).
+    # 1 + 3*2^-8 is a tie between mantissas 1 and 2: even (2) wins.
+    assert b.tolist() == [0x3F80, 0xC020, 0x3F80, 0x3F81, 0x3F82]
+
+
+@pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
+def test_routing_shapes_and_determinism(c):
+    cfg = ei.CONFIGS[c]
+    i1, w1 = ei.make_routing(cfg, 0)
+    i2, w2 = ei.make_routing(cfg, 0)
+    assert i1.shape == (cfg.N, cfg.K) and i1.dtype == np.int32
+    assert w1.shape == (cfg.N, cfg.K) and w1.dtype == np.float32
+    assert np.array_equal(i1, i2) and np.array_equal(w1, w2)
+    valid = i1 >= 0
+    assert np.all(i1[valid] < cfg.E)
+    # distinct experts within a row
+    for row in i1[:256]:
+        r = row[row >= 0]
+        assert len(set(r.tolist())) == len(r)
+    # renormalised weights (before masking)
+    if cfg.mask_frac == 0:
+        assert np.allclose(w1.sum(1), 1.0, atol=1e-6)
+        assert np.all(w1 > 0)
+        # slots in descending weight order
+        assert np.all(np.diff(w1, axis=1) <= 1e-7)
+
+
+def test_grouped_gating_limits_groups():
+    cfg = ei.CONFIGS[3]
+    idx, _ = ei.make_routing(cfg, 0)
+    groups = idx // (cfg.E // cfg.n_groups)
+    assert max(len(set(r)) for r in groups.tolist()) <= cfg.topk_groups
+
+
+def test_zipf_mask_and_skew():
+    cfg = ei.CONFIGS[5]
+    idx, w = ei.make_routing(cfg, 0)
+    n_mask = int(round(cfg.mask_frac * cfg.N * cfg.K))
+    assert (idx == -1).sum() == n_mask == 6554
+    assert np.all(w[idx == -1] == 0)
+    counts = np.bincount(idx[idx >= 0], minlength=cfg.E)
+    assert counts.argmax() == 0 and counts[0] > 6000
+    assert np.all(np.diff(counts[:8]) < 0)
+
+
+def test_x_distribution_small():
+    x = ei.make_x(64, 256, seed=3)
+    f = (x.astype(np.uint32) << 16).view(np.float32)
+    assert x.dtype == np.uint16 and x.shape == (64, 256)
+    assert abs(f.mean()) < 0.05 and abs(f.std() - 1) < 0.05
