@@ -1,0 +1,313 @@
+// The C ABI declared in include/ep.h: argument checks, workspace carving and
+// kernel launches. No entry point allocates, frees or synchronises.
+#include <stdint.h>
+
+#include "ep.h"
+#include "kernels.cuh"
+
+namespace {
+
+using namespace ep;
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int64_t kEntriesPerCta = 6144;
+constexpr int kMaxLayoutCtas = 256;
+
+inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool sizes_ok(int N, int K, int E, int R) {
+  if (N < 0 || K < 1 || K > EP_MAX_TOPK || E < 1 || E > EP_MAX_EXPERTS) return false;
+  if (R < 1 || R > E || E % R != 0) return false;
+  if (static_cast<int64_t>(N) * K > INT32_MAX || static_cast<int64_t>(N) * R > INT32_MAX) return false;
+  return true;
+}
+
+bool hidden_ok(int H, int use_fp8) {
+  if (H < 8 || H > EP_MAX_HIDDEN || H % 8 != 0) return false;
+  if (use_fp8 && H % 128 != 0) return false;
+  return true;
+}
+
+int layout_ctas_wanted(int N, int K) {
+  const int64_t entries = static_cast<int64_t>(N) * K;
+  int64_t g = (entries + kEntriesPerCta - 1) / kEntriesPerCta;
+  if (g < 1) g = 1;
+  if (g > kMaxLayoutCtas) g = kMaxLayoutCtas;
+  return static_cast<int>(g);
+}
+
+// Layout workspace: [barrier 256 B][chunk counts G x C int32].
+struct LayoutWs {
+  size_t barrier, chunk, total;
+};
+LayoutWs layout_ws(int N, int K, int E, int R) {
+  LayoutWs w;
+  w.barrier = 0;
+  w.chunk = 256;
+  w.total = w.chunk + align256(sizeof(int32_t) * static_cast<size_t>(layout_ctas_wanted(N, K)) * (E + R));
+  return w;
+}
+
+// Low-latency workspace: header, counts, ranges, slot map, chunk counts, barrier.
+struct LLWs {
+  size_t hdr, count, range, slot, chunk, barrier, total;
+};
+LLWs ll_ws(int N, int K, int E, int R) {
+  LLWs w;
+  w.hdr = 0;
+  w.count = 256;
+  w.range = w.count + align256(sizeof(int32_t) * E);
+  w.slot = w.range + align256(sizeof(int64_t) * static_cast<size_t>(E) * R);
+  w.chunk = w.slot + align256(sizeof(int32_t) * static_cast<size_t>(N) * K);
+  w.barrier = w.chunk + align256(sizeof(int32_t) * static_cast<size_t>(R) * E);
+  w.total = w.barrier + 256;
+  return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+bool layout_ok(const ep_layout_t* L) {
+  if (!L) return false;
+  if (!sizes_ok(L->num_tokens, L->num_topk, L->num_experts, L->num_ranks)) return false;
+  if (L->num_tokens > 0 && !L->topk_idx) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_version(void) { return kVersion; }
+
+const char* ep_error_string(int c) {
+  switch (c) {
+    case EP_OK: return "ok";
+    case EP_ERR_INVALID_ARG: return "invalid argument";
+    case EP_ERR_ALIGNMENT: return "row buffer not 16-byte aligned";
+    case EP_ERR_WORKSPACE: return "workspace missing or too small";
+    case EP_ERR_LL_CAPACITY: return "low-latency: tokens per rank exceed max_tokens_per_rank";
+    case EP_ERR_CUDA: return "CUDA runtime or launch error";
+    case EP_ERR_UNSUPPORTED: return "device lacks a required feature";
+    default: break;
+  }
+  if (c > 0) {
+    if (c & EP_ST_BAD_INDEX) return "status: top-k index outside [-1, num_experts)";
+    if (c & EP_ST_CAPACITY) return "status: row beyond buffer capacity skipped";
+    if (c & EP_ST_LL_OVERFLOW) return "status: low-latency expert region overflow";
+    if (c & EP_ST_TIMEOUT) return "status: bounded in-kernel wait timed out";
+    if (c & EP_ST_NOT_SENT) return "status: low-latency receive/combine without a send";
+    if (c & EP_ST_MISMATCH) return "status: low-latency shapes differ from the send";
+  }
+  return "unknown code";
+}
+
+size_t ep_layout_workspace_bytes(int N, int K, int E, int R) {
+  if (!sizes_ok(N, K, E, R)) return 0;
+  return layout_ws(N, K, E, R).total;
+}
+
+int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status,
+                           void* stream) {
+  if (!layout_ok(L)) return EP_ERR_INVALID_ARG;
+  const int N = L->num_tokens, K = L->num_topk, E = L->num_experts, R = L->num_ranks;
+  if (!L->num_tokens_per_rank || !L->num_tokens_per_expert || !L->rank_offset || !L->expert_offset)
+    return EP_ERR_INVALID_ARG;
+  if (N > 0 && (!L->is_token_in_rank || !L->rank_slot || !L->expert_slot)) return EP_ERR_INVALID_ARG;
+  const LayoutWs w = layout_ws(N, K, E, R);
+  if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  int G = layout_ctas_wanted(N, K);
+  const int gmax = layout_max_ctas(E, R, true);
+  if (gmax < 1) return EP_ERR_UNSUPPORTED;
+  if (G > gmax) G = gmax;
+  LayoutParams p{};
+  p.idx = L->topk_idx;
+  p.N = N; p.K = K; p.E = E; p.R = R; p.L = E / R;
+  p.tokens_per_cta = (N + G - 1) / G;
+  if (p.tokens_per_cta < 1) p.tokens_per_cta = 1;
+  p.per_rank = L->num_tokens_per_rank;
+  p.per_expert = L->num_tokens_per_expert;
+  p.mask = L->is_token_in_rank;
+  p.rank_off = L->rank_offset;
+  p.expert_off = L->expert_offset;
+  p.rank_slot = L->rank_slot;
+  p.expert_slot = L->expert_slot;
+  p.ws_chunk = at<int32_t>(workspace, w.chunk);
+  p.ws_barrier = at<unsigned>(workspace, w.barrier);
+  p.status = status;
+  return cuda_rc(launch_layout(p, G, true, false, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int use_fp8, const float* topk_weights,
+                const ep_recv_buffer_t* rank_buf, const ep_recv_buffer_t* expert_buf, int32_t* status,
+                void* stream) {
+  if (!layout_ok(L) || !hidden_ok(hidden, use_fp8)) return EP_ERR_INVALID_ARG;
+  const int N = L->num_tokens, K = L->num_topk, E = L->num_experts, R = L->num_ranks;
+  if (N > 0 && !x) return EP_ERR_INVALID_ARG;
+  if (!aligned16(x)) return EP_ERR_ALIGNMENT;
+  DispatchParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.N = N; p.K = K; p.H = hidden; p.E = E; p.R = R; p.L = E / R;
+  p.idx = L->topk_idx;
+  p.w = topk_weights;
+  p.status = status;
+  p.overflow_bit = EP_ST_CAPACITY;
+  if (rank_buf && rank_buf->x) {
+    if (N > 0 && !L->rank_slot) return EP_ERR_INVALID_ARG;
+    if (rank_buf->capacity < 0) return EP_ERR_INVALID_ARG;
+    if (rank_buf->topk_weights && !topk_weights) return EP_ERR_INVALID_ARG;
+    if (!aligned16(rank_buf->x) || (use_fp8 && rank_buf->scales && !aligned16(rank_buf->scales)))
+      return EP_ERR_ALIGNMENT;
+    p.rank_slot = L->rank_slot;
+    p.rank_x = static_cast<uint8_t*>(rank_buf->x);
+    p.rank_scales = use_fp8 ? rank_buf->scales : nullptr;
+    p.rank_src = rank_buf->src_idx;
+    p.rank_topk_idx = rank_buf->topk_idx;
+    p.rank_topk_w = rank_buf->topk_weights;
+    p.rank_cap = rank_buf->capacity;
+  }
+  if (expert_buf && expert_buf->x) {
+    if (N > 0 && !L->expert_slot) return EP_ERR_INVALID_ARG;
+    if (expert_buf->capacity < 0) return EP_ERR_INVALID_ARG;
+    if (!aligned16(expert_buf->x) || (use_fp8 && expert_buf->scales && !aligned16(expert_buf->scales)))
+      return EP_ERR_ALIGNMENT;
+    p.expert_slot = L->expert_slot;
+    p.exp_x = static_cast<uint8_t*>(expert_buf->x);
+    p.exp_scales = use_fp8 ? expert_buf->scales : nullptr;
+    p.exp_src = expert_buf->src_idx;
+    p.exp_cap = expert_buf->capacity;
+  }
+  if (!p.rank_x && !p.exp_x) return EP_OK;
+  return cuda_rc(launch_dispatch(p, use_fp8 != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,
+               const float* topk_weights, void* out, int32_t* status, void* stream) {
+  if (!layout_ok(L) || !hidden_ok(hidden, 0) || y_rows < 0) return EP_ERR_INVALID_ARG;
+  const int N = L->num_tokens;
+  if (N > 0 && (!L->expert_slot || !topk_weights || !out || (!expert_y && y_rows > 0)))
+    return EP_ERR_INVALID_ARG;
+  if (!aligned16(expert_y) || !aligned16(out)) return EP_ERR_ALIGNMENT;
+  CombineParams p{};
+  p.y = static_cast<const uint16_t*>(expert_y);
+  p.y_rows = y_rows;
+  p.slot = L->expert_slot;
+  p.w = topk_weights;
+  p.out = static_cast<uint16_t*>(out);
+  p.N = N; p.K = L->num_topk; p.H = hidden;
+  p.status = status;
+  return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t ep_ll_workspace_bytes(int N, int K, int E, int R, int T) {
+  if (!sizes_ok(N, K, E, R) || T < 1) return 0;
+  return ll_ws(N, K, E, R).total;
+}
+
+static int ll_common_checks(int N, int K, int E, int R, int T) {
+  if (!sizes_ok(N, K, E, R) || T < 1) return EP_ERR_INVALID_ARG;
+  if (N % R != 0) return EP_ERR_INVALID_ARG;
+  if (N / R > T) return EP_ERR_LL_CAPACITY;
+  if (static_cast<int64_t>(E) * R * T > INT32_MAX) return EP_ERR_INVALID_ARG;
+  return EP_OK;
+}
+
+int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, int H, int E, int R, int T,
+                        int use_fp8, void* recv_x, float* recv_scales, int32_t* recv_src, void* workspace,
+                        size_t workspace_bytes, int32_t* status, void* stream) {
+  int rc = ll_common_checks(N, K, E, R, T);
+  if (rc != EP_OK) return rc;
+  if (!hidden_ok(H, use_fp8)) return EP_ERR_INVALID_ARG;
+  if (!recv_x || (N > 0 && (!x || !topk_idx))) return EP_ERR_INVALID_ARG;
+  if (use_fp8 && !recv_scales) return EP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(recv_x) || (use_fp8 && !aligned16(recv_scales))) return EP_ERR_ALIGNMENT;
+  const LLWs w = ll_ws(N, K, E, R);
+  if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  const int gmax = layout_max_ctas(E, R, false);
+  if (gmax < 1 || R > gmax) return EP_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  LayoutParams lp{};
+  lp.idx = topk_idx;
+  lp.N = N; lp.K = K; lp.E = E; lp.R = R; lp.L = E / R;
+  lp.tokens_per_cta = (N / R > 0) ? N / R : 1;
+  lp.per_expert = at<int32_t>(workspace, w.count);
+  lp.expert_slot = at<int32_t>(workspace, w.slot);
+  lp.ll_cap = static_cast<int64_t>(R) * T;
+  lp.ll_range = at<int64_t>(workspace, w.range);
+  lp.ll_hdr = at<LLHeader>(workspace, w.hdr);
+  lp.hdr_value = LLHeader{kMagicSent, N, K, E, R, T, H, use_fp8, 0};
+  lp.ws_chunk = at<int32_t>(workspace, w.chunk);
+  lp.ws_barrier = at<unsigned>(workspace, w.barrier);
+  lp.status = status;
+  rc = cuda_rc(launch_layout(lp, R, false, true, s));
+  if (rc != EP_OK) return rc;
+
+  DispatchParams dp{};
+  dp.x = static_cast<const uint16_t*>(x);
+  dp.N = N; dp.K = K; dp.H = H; dp.E = E; dp.R = R; dp.L = E / R;
+  dp.idx = topk_idx;
+  dp.expert_slot = at<int32_t>(workspace, w.slot);
+  dp.exp_x = static_cast<uint8_t*>(recv_x);
+  dp.exp_scales = use_fp8 ? recv_scales : nullptr;
+  dp.exp_src = recv_src;
+  dp.exp_cap = static_cast<int64_t>(E) * R * T;
+  dp.exp_src_is_token = 1;
+  dp.overflow_bit = EP_ST_LL_OVERFLOW;
+  dp.status = status;
+  return cuda_rc(launch_dispatch(dp, use_fp8 != 0, s));
+}
+
+int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int N, int K, int E, int R, int T,
+                        int32_t* recv_count, int64_t* layout_range, int32_t* status, void* stream) {
+  int rc = ll_common_checks(N, K, E, R, T);
+  if (rc != EP_OK) return rc;
+  if (!recv_count) return EP_ERR_INVALID_ARG;
+  const LLWs w = ll_ws(N, K, E, R);
+  if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  void* ws = workspace;
+  LLRecvParams p{};
+  p.hdr = at<LLHeader>(ws, w.hdr);
+  p.count = at<int32_t>(ws, w.count);
+  p.range = at<int64_t>(ws, w.range);
+  p.expect = LLHeader{kMagicSent, N, K, E, R, T, 0, 0, 0};
+  p.recv_count = recv_count;
+  p.layout_range = layout_range;
+  p.status = status;
+  return cuda_rc(launch_ll_recv(p, E, R, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* workspace, size_t workspace_bytes,
+                  int N, int K, int H, int E, int R, int T, void* out, int32_t* status, void* stream) {
+  int rc = ll_common_checks(N, K, E, R, T);
+  if (rc != EP_OK) return rc;
+  if (!hidden_ok(H, 0)) return EP_ERR_INVALID_ARG;
+  if (!expert_y || (N > 0 && (!topk_weights || !out))) return EP_ERR_INVALID_ARG;
+  if (!aligned16(expert_y) || !aligned16(out)) return EP_ERR_ALIGNMENT;
+  const LLWs w = ll_ws(N, K, E, R);
+  if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  void* ws = const_cast<void*>(workspace);
+  CombineParams p{};
+  p.y = static_cast<const uint16_t*>(expert_y);
+  p.y_rows = static_cast<int64_t>(E) * R * T;
+  p.slot = at<int32_t>(ws, w.slot);
+  p.w = topk_weights;
+  p.out = static_cast<uint16_t*>(out);
+  p.N = N; p.K = K; p.H = H;
+  p.ll_hdr = at<LLHeader>(ws, w.hdr);
+  p.ll_expect = LLHeader{kMagicSent, N, K, E, R, T, H, 0, 0};
+  p.status = status;
+  return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_fp8_e4m3_encode(const float* in, uint8_t* out, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!in || !out))) return EP_ERR_INVALID_ARG;
+  return cuda_rc(launch_e4m3_encode(in, out, n, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Combine on sm_103a: gather each token's expert outputs back and take the
+// router-weighted top-k sum.
+//
+// What it computes ("DeepEP Ascend deep dive", "Two Transfers": results come
+// back along the same path and are weighted by router score and summed;
+// "DeepEP lesson 14", practice task: out_i = sum_k w_ik * y_ik):
+//   out[t] = bf16_rn( fma(w[t,K-1], y[slot[t,K-1]], ... fma(w[t,0], y[slot[t,0]], +0)) )
+// over unmasked slots, in slot order, one fp32 fused multiply-add per term.
+//
+// Design (HBM-bound, read-heavy: K rows read, one row written per token).
+// One block per token (grid-stride). The token's slots and weights go to
+// shared memory once; each thread then owns 16-byte vectors of the row and,
+// for up to 8 slots at a time, issues all their loads before the FMAs, so K
+// independent 16-byte reads per thread are in flight. The reduction happens
+// in registers as the rows arrive: no intermediate buffer, no second pass.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kChunk = 8;
+
+__device__ __forceinline__ void fma8(float* acc, float w, const uint4& v) {
+  acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
+  acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
+  acc[2] = __fmaf_rn(w, bf16_lo(v.y), acc[2]);
+  acc[3] = __fmaf_rn(w, bf16_hi(v.y), acc[3]);
+  acc[4] = __fmaf_rn(w, bf16_lo(v.z), acc[4]);
+  acc[5] = __fmaf_rn(w, bf16_hi(v.z), acc[5]);
+  acc[6] = __fmaf_rn(w, bf16_lo(v.w), acc[6]);
+  acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
+}
+
+__device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b) {
+  return a.N == b.N && a.K == b.K && a.E == b.E && a.R == b.R && a.T == b.T;
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+  __shared__ int32_t s_row[EP_MAX_TOPK];
+  __shared__ float s_w[EP_MAX_TOPK];
+  __shared__ int s_ok;
+  const int tid = threadIdx.x;
+  const int K = p.K, H = p.H;
+  if (p.ll_hdr) {
+    if (tid == 0) {
+      const LLHeader h = *p.ll_hdr;
+      int ok = (h.magic == kMagicSent || h.magic == kMagicReceived) ? 1 : 0;
+      if (!ok) {
+        if (blockIdx.x == 0) flag(p.status, EP_ST_NOT_SENT);
+      } else if (!same_shape(h, p.ll_expect)) {
+        ok = 0;
+        if (blockIdx.x == 0) flag(p.status, EP_ST_MISMATCH);
+      }
+      s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) return;
+  }
+  const int nvec = H / 8;
+  for (int64_t t = blockIdx.x; t < p.N; t += gridDim.x) {
+    if (tid < K) {
+      int32_t row = __ldg(p.slot + t * K + tid);
+      if (row >= p.y_rows) {
+        flag(p.status, EP_ST_CAPACITY);
+        row = -1;
+      }
+      s_row[tid] = row;
+      s_w[tid] = __ldg(p.w + t * K + tid);
+    }
+    __syncthreads();
+    uint16_t* out = p.out + t * H;
+    for (int v = tid; v < nvec; v += kThreads) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int k0 = 0; k0 < K; k0 += kChunk) {
+        uint4 yv[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          const int k = k0 + j;
+          const int32_t row = (k < K) ? s_row[k] : -1;
+          if (row >= 0)
+            yv[j] = __ldg(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
+        }
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          const int k = k0 + j;
+          const int32_t row = (k < K) ? s_row[k] : -1;
+          if (row >= 0) fma8(acc, s_w[k], yv[j]);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4*>(out)[v] = o;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
+  if (p.N <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t full = static_cast<int64_t>(sms) * 16;
+  const int grid = static_cast<int>(p.N < full ? p.N : full);
+  combine_kernel<<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,97 @@
+// Kernel parameter blocks and launchers (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ep {
+
+// Workspace header of the low-latency path: written by the send, checked by
+// the receive and the combine.
+struct LLHeader {
+  unsigned long long magic;
+  int32_t N, K, E, R, T, H, use_fp8, pad;
+};
+constexpr unsigned long long kMagicSent = 0x4C4C2D53454E5421ull;      // "LL-SENT!"
+constexpr unsigned long long kMagicReceived = 0x4C4C2D5245435644ull;  // "LL-RECVD"
+
+struct LayoutParams {
+  const int32_t* idx;  // [N, K]
+  int N, K, E, R, L;
+  int tokens_per_cta;
+  // normal-mode outputs
+  int32_t* per_rank;
+  int32_t* per_expert;
+  uint8_t* mask;
+  int32_t* rank_off;
+  int32_t* expert_off;
+  int32_t* rank_slot;
+  int32_t* expert_slot;  // low-latency mode: the slot map (row e * ll_cap + j)
+  // low-latency mode outputs
+  int64_t ll_cap;
+  int64_t* ll_range;   // [E, R]
+  LLHeader* ll_hdr;
+  LLHeader hdr_value;
+  // scratch
+  int32_t* ws_chunk;   // [G, C]
+  unsigned* ws_barrier;
+  int32_t* status;
+};
+
+struct DispatchParams {
+  const uint16_t* x;  // [N, H] BF16
+  int N, K, H, E, R, L;
+  const int32_t* idx;
+  const float* w;
+  const int32_t* expert_slot;  // [N, K] destination rows (low-latency: slot map)
+  const int32_t* rank_slot;    // [N, R] or null
+  // per-rank buffer (null x: skip)
+  uint8_t* rank_x;
+  float* rank_scales;
+  int32_t* rank_src;
+  int32_t* rank_topk_idx;
+  float* rank_topk_w;
+  int64_t rank_cap;
+  // expert-major buffer (null x: skip)
+  uint8_t* exp_x;
+  float* exp_scales;
+  int32_t* exp_src;
+  int64_t exp_cap;
+  int exp_src_is_token;  // 1: exp_src[row] = t (low-latency recv_src); 0: t * K + k
+  int overflow_bit;      // status bit for a row beyond exp_cap
+  int32_t* status;
+};
+
+struct CombineParams {
+  const uint16_t* y;     // [y_rows, H] BF16
+  int64_t y_rows;
+  const int32_t* slot;   // [N, K]
+  const float* w;        // [N, K]
+  uint16_t* out;         // [N, H]
+  int N, K, H;
+  const LLHeader* ll_hdr;  // low-latency: the send's header (null in normal mode)
+  LLHeader ll_expect;
+  int32_t* status;
+};
+
+struct LLRecvParams {
+  LLHeader* hdr;
+  const int32_t* count;   // [E]
+  const int64_t* range;   // [E, R]
+  LLHeader expect;
+  int32_t* recv_count;
+  int64_t* layout_range;
+  int32_t* status;
+};
+
+// Launchers: return cudaSuccess or the launch error.
+size_t layout_smem_bytes(int E, int R, bool with_rank);
+int layout_max_ctas(int E, int R, bool with_rank);  // co-resident limit (device-specific)
+cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll, cudaStream_t s);
+
+cudaError_t launch_dispatch(const DispatchParams& p, bool fp8, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s);
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
+
+}  // namespace ep

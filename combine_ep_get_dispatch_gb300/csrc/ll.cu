@@ -1,0 +1,76 @@
+// Low-latency receive phase and the element-wise E4M3 encoder.
+//
+// The receive phase is the deferred second launch of the low-latency
+// dispatch ("How DeepEP enables hook-based overlapping", "Two-Phase Kernel
+// Architecture": the receive phase runs when the hook is called; "DeepEP V1
+// (legacy) guide", section 6.3: the hook guarantees the data has arrived and
+// the per-expert receive counts are returned). On one GPU the send already
+// placed the rows; the receive checks that a send with the same shapes
+// filled the workspace, then publishes the per-expert counts and the
+// per-(expert, source rank) ranges, and marks the workspace consumed. It
+// never waits on another launch: it must be ordered after the send on the
+// stream.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kRecvThreads = 1024;
+
+__global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParams p, int E, int R) {
+  __shared__ int s_ok;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    const LLHeader h = *p.hdr;  // written by an earlier launch on this stream
+    int ok = 1;
+    if (h.magic != kMagicSent) {
+      ok = 0;
+      flag(p.status, EP_ST_NOT_SENT);
+    } else if (h.N != p.expect.N || h.K != p.expect.K || h.E != p.expect.E || h.R != p.expect.R ||
+               h.T != p.expect.T) {
+      ok = 0;
+      flag(p.status, EP_ST_MISMATCH);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  for (int e = tid; e < E; e += kRecvThreads) p.recv_count[e] = p.count[e];
+  if (p.layout_range) {
+    const int64_t n = static_cast<int64_t>(E) * R;
+    for (int64_t i = tid; i < n; i += kRecvThreads) p.layout_range[i] = p.range[i];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    p.hdr->magic = kMagicReceived;
+  }
+}
+
+__global__ void e4m3_encode_kernel(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    out[i] = static_cast<uint8_t>(pack_e4m3x2(in[i], 0.0f) & 0xFFu);
+}
+
+}  // namespace
+
+cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s) {
+  ll_recv_kernel<<<1, kRecvThreads, 0, s>>>(p, E, R);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  e4m3_encode_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, s>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace ep

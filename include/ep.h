@@ -1,0 +1,296 @@
+/*
+ * ep.h - C ABI of a single-GPU (GB300, sm_103a) MoE token layout, dispatch
+ * and combine library.
+ *
+ * What it computes follows the DeepEP write-ups:
+ *   - "DeepEP V1 (legacy) guide" (zskr.cn), section 5 (normal kernels:
+ *     get_dispatch_layout, dispatch, combine), section 6 (low-latency
+ *     kernels: fixed-shape receive buffer, receive counts, receive hook);
+ *   - "How DeepEP enables hook-based overlapping" (instagit.com), sections
+ *     "Two-Phase Kernel Architecture" and "Compute Stream vs. Communication
+ *     Stream" (send and receive as two launches; the launch stream);
+ *   - "DeepEP Ascend deep dive" (kongchang.com), sections "Two Transfers" and
+ *     "Dispatch's Three Phases" (one copy per destination rank; the
+ *     expert-major "expand" layout; the weighted top-k sum of combine).
+ *
+ * Expert-parallel ranks are logical partitions of one GPU's memory: R ranks,
+ * E experts, expert e lives on rank e / (E / R). Tokens are split
+ * contiguously over the R source ranks, so "source rank, then token index"
+ * order is global token order.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller unless
+ *     stated otherwise. The library never allocates or frees memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call only enqueues work on it and returns; nothing synchronises with
+ *     the host. Outputs are ready when the stream reaches that point.
+ *   - Return value: EP_OK, or a negative EP_ERR_* code for an error the host
+ *     can see (bad argument, bad alignment, too-small workspace, a CUDA
+ *     launch error). Nothing is enqueued when an error is returned.
+ *   - `status` (may be NULL) points to one device int32. Kernels OR EP_ST_*
+ *     bits into it for data-dependent conditions (an expert index out of
+ *     range, a destination row beyond a buffer's capacity, ...). The
+ *     offending row is skipped; no kernel traps. The caller zeroes it.
+ *   - BF16 data is passed as raw 16-bit words, E4M3 data as bytes.
+ *   - Row buffers (x, receive buffers, expert outputs, out) must be 16-byte
+ *     aligned, and hidden * element size must be a multiple of 16 bytes.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---------------------------------------------------- */
+#define EP_OK 0
+#define EP_ERR_INVALID_ARG (-1) /* null pointer, size out of range, E % R != 0, ... */
+#define EP_ERR_ALIGNMENT (-2)   /* a row buffer is not 16-byte aligned */
+#define EP_ERR_WORKSPACE (-3)   /* workspace missing or smaller than required */
+#define EP_ERR_LL_CAPACITY (-4) /* low-latency: N / R tokens per rank exceed T */
+#define EP_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+#define EP_ERR_UNSUPPORTED (-6) /* device lacks a required feature */
+
+/* ---- device status bits ---------------------------------------------- */
+#define EP_ST_BAD_INDEX 0x1   /* a top-k index outside [-1, E): treated as -1 */
+#define EP_ST_CAPACITY 0x2    /* a row did not fit the given buffer: skipped */
+#define EP_ST_LL_OVERFLOW 0x4 /* low-latency: a row beyond an expert's R*T region */
+#define EP_ST_TIMEOUT 0x8     /* a bounded in-kernel wait gave up */
+#define EP_ST_NOT_SENT 0x10   /* low-latency receive without a matching send */
+#define EP_ST_MISMATCH 0x20   /* low-latency shapes differ from those of the send */
+
+/* ---- limits ---------------------------------------------------------- */
+#define EP_MAX_EXPERTS 1024
+#define EP_MAX_TOPK 32
+#define EP_MAX_HIDDEN 16384
+
+/*
+ * The routing layout of one batch: the handle that dispatch and combine take.
+ * The caller allocates every array and fills in the pointers and sizes;
+ * ep_get_dispatch_layout writes the arrays. Reusing a filled handle skips the
+ * layout ("cached dispatch", DeepEP V1 guide section 5.2(4)).
+ *
+ *   topk_idx              [N, K] int32  in: expert of each top-k slot, -1 = none
+ *   num_tokens_per_rank   [R]    int32  tokens sent to each rank (one copy per rank)
+ *   num_tokens_per_expert [E]    int32  (token, slot) pairs routed to each expert
+ *   is_token_in_rank      [N, R] uint8  1 if some expert of the token lives on the rank
+ *   rank_offset           [R+1]  int32  exclusive prefix sum of num_tokens_per_rank
+ *   expert_offset         [E+1]  int32  exclusive prefix sum of num_tokens_per_expert
+ *   rank_slot             [N, R] int32  row of the token in the per-rank buffer, or -1
+ *   expert_slot           [N, K] int32  row of (token, slot) in the expert-major buffer, or -1
+ *
+ * Slots are deterministic: within a rank (or an expert) rows are in token
+ * order (and top-k order for repeated experts), ranks (experts) in index
+ * order.
+ */
+typedef struct ep_layout {
+  int32_t num_tokens;  /* N >= 0 */
+  int32_t num_topk;    /* 1 <= K <= EP_MAX_TOPK */
+  int32_t num_experts; /* 1 <= E <= EP_MAX_EXPERTS */
+  int32_t num_ranks;   /* 1 <= R <= E, E % R == 0 */
+  const int32_t* topk_idx;
+  int32_t* num_tokens_per_rank;
+  int32_t* num_tokens_per_expert;
+  uint8_t* is_token_in_rank;
+  int32_t* rank_offset;
+  int32_t* expert_offset;
+  int32_t* rank_slot;
+  int32_t* expert_slot;
+} ep_layout_t;
+
+/*
+ * One receive buffer of ep_dispatch. Rows are packed: the per-rank buffer by
+ * rank_offset, the expert-major buffer by expert_offset.
+ *   x             [capacity, H]       BF16 words, or E4M3 bytes when use_fp8
+ *   scales        [capacity, H/128]   fp32 (use_fp8 only; may be NULL to skip)
+ *   src_idx       [capacity]          int32, may be NULL. Per-rank buffer: the
+ *                                     token index t. Expert-major: t * K + k.
+ *   topk_idx      [capacity, K]       int32, may be NULL; per-rank buffer only:
+ *                                     the local expert id (e - r * E/R) of each
+ *                                     slot whose expert lives on this rank, else -1
+ *   topk_weights  [capacity, K]       fp32, may be NULL; per-rank buffer only:
+ *                                     the slot's router weight, or 0
+ *   capacity      rows allocated; rows at or beyond it are skipped and flagged
+ *                 EP_ST_CAPACITY. N * min(K, R) (per-rank) and N * K
+ *                 (expert-major) always suffice without reading the counts.
+ */
+typedef struct ep_recv_buffer {
+  void* x;
+  float* scales;
+  int32_t* src_idx;
+  int32_t* topk_idx;
+  float* topk_weights;
+  int64_t capacity;
+} ep_recv_buffer_t;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int ep_version(void);
+
+/* A short English description of a return code (negative) or of the lowest
+ * set status bit (positive). Static storage; never NULL. */
+const char* ep_error_string(int code_or_status);
+
+/*
+ * Bytes of device workspace ep_get_dispatch_layout needs for these sizes.
+ * Depends only on the arguments (not on the device).
+ */
+size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks);
+
+/*
+ * Routing layout: counts, the per-rank mask and deterministic prefix-sum
+ * slots (DeepEP V1 guide section 5.2(1): get_dispatch_layout returns
+ * num_tokens_per_rank, num_tokens_per_expert and is_token_in_rank; "DeepEP
+ * Ascend deep dive", "Two Transfers": a rank receives a token once even when
+ * several of its experts live there; "Dispatch's Three Phases", phase 3: the
+ * receive-source map that combine follows back).
+ *
+ *   L          handle: sizes, topk_idx and the output arrays (see ep_layout_t)
+ *   workspace  device scratch of at least ep_layout_workspace_bytes(...)
+ *              bytes; its contents on entry do not matter (the call resets
+ *              what it needs). Must not be used by another call in flight.
+ *   status     EP_ST_BAD_INDEX when an index lies outside [-1, E) (the slot
+ *              is treated as -1); EP_ST_TIMEOUT if an internal grid-wide wait
+ *              gave up (outputs then invalid).
+ * Runs as one cooperative launch.
+ */
+int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes,
+                           int32_t* status, void* stream);
+
+/*
+ * Dispatch: copy each token's hidden row x[t] into the per-rank receive
+ * buffer (row rank_slot[t, r] for every rank r of its mask: one copy per
+ * rank) and into the expert-major buffer (row expert_slot[t, k] for every
+ * unmasked slot k: one copy per chosen expert), optionally quantised once to
+ * FP8 E4M3 with one fp32 scale per 128 channels: s = amax / 448 (round to
+ * nearest), q = e4m3(x / s) rounded to nearest even and saturated to +-448;
+ * an all-zero block has s = 0 and zero codes.
+ * (DeepEP V1 guide sections 5.1 and 5.2(6); "DeepEP Ascend deep dive",
+ * "Dispatch's Three Phases": the expert-major expand layout and FP8 E4M3 with
+ * a scale travelling with each token.)
+ *
+ *   L             a handle filled by ep_get_dispatch_layout
+ *   x             [N, hidden] BF16
+ *   hidden        H: a multiple of 8 (BF16) or of 128 (FP8), <= EP_MAX_HIDDEN
+ *   use_fp8       0: rows are copied as BF16; 1: rows are E4M3 + scales
+ *   topk_weights  [N, K] fp32; needed only for rank_buf->topk_weights
+ *   rank_buf      per-rank receive buffer, or NULL to skip the per-rank copy
+ *   expert_buf    expert-major receive buffer, or NULL to skip it
+ *   status        EP_ST_CAPACITY for rows beyond a buffer's capacity
+ */
+int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int use_fp8,
+                const float* topk_weights, const ep_recv_buffer_t* rank_buf,
+                const ep_recv_buffer_t* expert_buf, int32_t* status, void* stream);
+
+/*
+ * Combine: gather the expert outputs back along the dispatch path and take
+ * the router-weighted sum: out[t] = bf16( sum over k = 0..K-1 with
+ * expert_slot[t, k] >= 0 of w[t, k] * y[expert_slot[t, k]] ), accumulated in
+ * fp32 with one fused multiply-add per term in slot order, starting from +0,
+ * rounded once to BF16 (nearest even). A token with every slot masked gets +0.
+ * ("DeepEP Ascend deep dive", "Two Transfers": results go back along the
+ * same path and are weighted by router scores and summed; "DeepEP lesson 14",
+ * practice task: out_i = sum_k w_ik * y_ik.)
+ *
+ *   L             a handle filled by ep_get_dispatch_layout
+ *   expert_y      [y_rows, hidden] BF16 expert outputs in expert-major order
+ *                 (row expert_slot[t, k] holds expert idx[t, k]'s output for t)
+ *   y_rows        rows of expert_y; slots at or beyond it are skipped and
+ *                 flagged EP_ST_CAPACITY
+ *   hidden        a multiple of 8, <= EP_MAX_HIDDEN
+ *   topk_weights  [N, K] fp32 router weights
+ *   out           [N, hidden] BF16
+ */
+int ep_combine(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,
+               const float* topk_weights, void* out, int32_t* status, void* stream);
+
+/*
+ * Bytes of device workspace the low-latency calls need. The workspace
+ * carries the routing from send to receive and combine (the "handle").
+ */
+size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int num_ranks,
+                             int max_tokens_per_rank);
+
+/*
+ * Low-latency dispatch, send phase (DeepEP V1 guide section 6.1/6.3;
+ * "How DeepEP enables hook-based overlapping", "Two-Phase Kernel
+ * Architecture": the send phase runs at once, the receive phase when the
+ * hook is called; "DeepEP lesson 14", low-latency call flow: receive buffer
+ * [num_local_experts, num_max_dispatch_tokens_per_rank * num_ranks, hidden]).
+ *
+ * Tokens are split contiguously over R source ranks, n = N / R each, with
+ * n <= T (else EP_ERR_LL_CAPACITY). Each (token, slot) with expert e >= 0 is
+ * written to expert e's fixed region of recv_x: rows are packed in token
+ * order at j = 0 .. count_e - 1 of [e][0 .. R*T). Rows j >= count_e are not
+ * written. Seen from rank r, its experts' regions form the pages' per-rank
+ * shape [E/R, R*T, H].
+ *
+ *   x            [N, hidden] BF16
+ *   topk_idx     [N, K] int32, -1 = no expert
+ *   recv_x       [E, R*T, hidden] BF16, or E4M3 when use_fp8
+ *   recv_scales  [E, R*T, hidden/128] fp32 (use_fp8 only)
+ *   recv_src     [E, R*T] int32: global token index of each written row
+ *   workspace    at least ep_ll_workspace_bytes(...) bytes; afterwards it
+ *                holds the routing that receive and combine use, until the
+ *                next send on it
+ *   status       EP_ST_BAD_INDEX as for the layout
+ * Enqueues two launches. The rows are in place when the stream reaches the
+ * end of this call; the counts are published by ep_ll_dispatch_recv.
+ */
+int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, int num_topk,
+                        int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
+                        int use_fp8, void* recv_x, float* recv_scales, int32_t* recv_src,
+                        void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Low-latency dispatch, receive phase: the deferred second launch (the
+ * "hook"). Publishes the per-expert receive counts and, per (expert, source
+ * rank), the range of rows that came from that source.
+ *
+ *   workspace     the workspace a send filled (same sizes)
+ *   recv_count    [E] int32: rows received by each expert
+ *   layout_range  [E, R] int64: (offset << 32) | count of the rows of expert
+ *                 e that came from source rank s (offsets are an exclusive
+ *                 scan over s); may be NULL
+ *   status        EP_ST_NOT_SENT if no send filled the workspace since the
+ *                 last receive; EP_ST_MISMATCH if the sizes differ from it
+ * Must be ordered after the send on the stream (same stream, or an event):
+ * the kernel checks the workspace once and never waits on another launch.
+ */
+int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int num_tokens, int num_topk,
+                        int num_experts, int num_ranks, int max_tokens_per_rank,
+                        int32_t* recv_count, int64_t* layout_range, int32_t* status, void* stream);
+
+/*
+ * Low-latency combine: out[t] = bf16( sum over k of w[t, k] * y[e][j(t, k)] )
+ * with the same fp32 fused multiply-add chain in slot order as ep_combine,
+ * where j(t, k) is the row the send gave (token, slot) in expert e's region.
+ * (DeepEP V1 guide section 6.1, low_latency_combine; "DeepEP lesson 14",
+ * low-latency call flow, step 4.)
+ *
+ *   expert_y      [E, R*T, hidden] BF16 expert outputs in the receive layout
+ *   topk_weights  [N, K] fp32
+ *   workspace     filled by the send of this batch (same sizes)
+ *   out           [N, hidden] BF16
+ *   status        EP_ST_NOT_SENT / EP_ST_MISMATCH as for the receive
+ */
+int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* workspace,
+                  size_t workspace_bytes, int num_tokens, int num_topk, int hidden,
+                  int num_experts, int num_ranks, int max_tokens_per_rank, void* out,
+                  int32_t* status, void* stream);
+
+/*
+ * Element-wise fp32 -> FP8 E4M3 conversion (round to nearest even, saturated
+ * to +-448, NaN -> NaN), the encoder the FP8 dispatch applies to x / s
+ * (DeepEP V1 guide section 5.2(6)). n >= 0 elements; in and out device
+ * pointers.
+ */
+int ep_fp8_e4m3_encode(const float* in, uint8_t* out, int64_t n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */
