@@ -160,6 +160,30 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
                            int32_t* status, void* stream);
 
 /*
+ * The routing layout for callers that cannot allocate device memory where
+ * they need it: code inside a host framework whose caching allocator owns the
+ * GPU's memory (a raw cudaMalloc bypasses its accounting and can fail once
+ * the pool holds most of HBM), plug-ins that are handed only their input and
+ * output buffers, and latency-critical loops where a cudaMalloc may
+ * synchronise the device. The DeepEP write-ups have no counterpart of this
+ * call; it is a convenience of this library.
+ *
+ * Same arguments and results as ep_get_dispatch_layout, without the
+ * workspace: the scratch lives in a 1 MiB array of device memory that the
+ * library holds on every GPU that loads it, until the process exits. Sizes
+ * whose ep_layout_workspace_bytes(...) exceeds 1 MiB return EP_ERR_WORKSPACE
+ * (for example E = R = 1024 with more than about 780,000 (token, slot)
+ * entries); no call allocates or frees memory.
+ *
+ * The first call on a device looks up that array's device address (once per
+ * device, with the device current); make that first call before any stream
+ * capture. Every call shares the array and it keeps the last call's contents
+ * (each launch resets what must start at zero). Calls that overlap on the GPU,
+ * such as calls on two streams with no ordering between them, race on it.
+ */
+int ep_get_dispatch_layout_noalloc(const ep_layout_t* L, int32_t* status, void* stream);
+
+/*
  * Dispatch: copy each token's hidden row x[t] into the per-rank receive
  * buffer (row rank_slot[t, r] for every rank r of its mask: one copy per
  * rank) and into the expert-major buffer (row expert_slot[t, k] for every
