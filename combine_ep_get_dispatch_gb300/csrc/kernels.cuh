@@ -19,6 +19,8 @@ struct LayoutParams {
   const int32_t* idx;  // [N, K]
   int N, K, E, R, L;
   int tokens_per_cta;
+  uint32_t magic_L, magic_K;  // ceil(2^32 / d) for d = L, K (0 when d == 1): exact n / d for n < 2^20
+  int bits_E, bits_R;         // bits of the largest expert / rank id
   // normal-mode outputs
   int32_t* per_rank;
   int32_t* per_expert;

@@ -10,29 +10,32 @@
 //   rank_slot[t, r]    rank_off[r] + #{t' < t with mask[t', r]}
 //
 // Design. The (token, slot) entries are cut into G contiguous chunks, one
-// per CTA, and each chunk into 16 contiguous warp ranges. A warp walks its
-// range 32 entries at a time; __match_any_sync groups the lanes that name the
-// same expert (or, for ranks, the first slot of a token on that rank), so the
-// rank of an entry among equal keys in the window is a popcount and one
-// leader lane bumps the warp's private counter: no atomics, and the order is
-// (token, slot) order by construction. Pass 1 counts; the per-chunk totals
-// go to global memory; one bounded grid barrier; every CTA then sums the
-// chunk totals before it (its prefix) and all of them (the totals), scans the
-// totals over experts and ranks, and pass 2 repeats the walk, now writing
-// slots. Launch-bound: the work is a few hundred KB of int32 traffic.
+// per CTA (up to 32 warps), and each chunk into contiguous warp ranges. A CTA
+// first stages its chunk's indices in shared memory in one coalesced pass,
+// coding each entry as (expert, rank, first-slot-of-the-token-on-that-rank);
+// divisions by E/R and K are multiply-highs. Pass 1 counts per warp with
+// shared-memory atomics. A shuffle scan across warps gives each warp its
+// prefix; the chunk totals go to global memory; one bounded grid barrier
+// (cooperative launch); every CTA then sums the chunk totals before it (its
+// prefix) and all of them (the totals) and scans the totals over experts and
+// ranks. Pass 2 walks the warp's range 32 entries at a time: ballots on the
+// key bits give each lane the lanes with the same expert (rank), so its
+// position among them is a popcount and one leader bumps the warp's counter.
+// No atomics decide an order: slots follow (token, slot) order by
+// construction. The kernel is bound by instruction latency, not memory: the
+// traffic is a few hundred KB of int32.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace ep {
 
-constexpr int kLayoutThreads = 512;
-constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kMaxLayoutThreads = 1024;
 
 // Exclusive scan of a[0..n) in shared memory, in place; returns the total.
-// All threads of the block must call it.
+// All threads of the block must call it; warp_tmp holds 32 ints.
 __device__ int block_exclusive_scan(int32_t* a, int n, int32_t* warp_tmp) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (n + kLayoutThreads - 1) / kLayoutThreads;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int per = (n + nthreads - 1) / nthreads;
   const int lo = min(n, tid * per), hi = min(n, lo + per);
   int s = 0;
   for (int i = lo; i < hi; ++i) s += a[i];
@@ -45,17 +48,17 @@ __device__ int block_exclusive_scan(int32_t* a, int n, int32_t* warp_tmp) {
   if (lane == 31) warp_tmp[w] = v;
   __syncthreads();
   if (w == 0) {
-    int x = lane < kLayoutWarps ? warp_tmp[lane] : 0;
+    int x = lane < nwarps ? warp_tmp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    if (lane < kLayoutWarps) warp_tmp[lane] = x;
+    if (lane < nwarps) warp_tmp[lane] = x;
   }
   __syncthreads();
   int run = (w > 0 ? warp_tmp[w - 1] : 0) + v - s;
-  const int total = warp_tmp[kLayoutWarps - 1];
+  const int total = warp_tmp[nwarps - 1];
   for (int i = lo; i < hi; ++i) {
     const int x = a[i];
     a[i] = run;
@@ -65,88 +68,186 @@ __device__ int block_exclusive_scan(int32_t* a, int n, int32_t* warp_tmp) {
   return total;
 }
 
-template <bool kRank, bool kLL>
-__global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutParams p) {
-  extern __shared__ int32_t sm[];
-  const int E = p.E, R = p.R, K = p.K, L = p.L;
-  const int C = E + (kRank ? R : 0);
-  int32_t* hist = sm;                        // [16][C]: counts, then running slots
-  int32_t* base = hist + kLayoutWarps * C;   // [C]: this chunk's prefix over earlier chunks
-  int32_t* tot = base + C;                   // [C]: totals, then their exclusive scan
-  int32_t* own = tot + C;                    // [C]: this chunk's own count
-  int32_t* tmp = own + C;                    // [32]
+// Entry code of one (token, slot): -1 for "no expert" (masked, or an index
+// outside [-1, E)), else e | r << 10 | first << 20, where r is expert e's
+// rank and `first` says that this slot is the token's first one on rank r
+// (the slot that carries the token's per-rank copy).
+constexpr int kFirstBit = 1 << 20;
+__device__ __forceinline__ int code_e(int c) { return c & 1023; }
+__device__ __forceinline__ int code_r(int c) { return (c >> 10) & 1023; }
 
+// Lanes of the warp whose `key` equals this lane's, among lanes with `valid`
+// set (0 for an invalid lane): one ballot per key bit. Keys lie in
+// [0, 2^nbits). All lanes must call it (nbits warp-uniform).
+__device__ __forceinline__ unsigned warp_peers(int key, bool valid, int nbits) {
+  unsigned m = __ballot_sync(0xffffffffu, valid);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (key >> b) & 1;
+    const unsigned v = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? v : ~v;
+  }
+  return valid ? m : 0u;
+}
+
+// n / d for 0 <= n < 2^20 by a multiply-high with magic = ceil(2^32 / d)
+// (magic 0 stands for d == 1); exact in that range for d <= 4096.
+__device__ __forceinline__ int fast_div(int n, uint32_t magic) {
+  return magic ? static_cast<int>(__umulhi(static_cast<unsigned>(n), magic)) : n;
+}
+
+template <bool kRank>
+__device__ __forceinline__ int entry_code_global(const LayoutParams& p, int64_t i, bool& bad) {
+  const int e = __ldg(p.idx + i);
+  if (e == -1) return -1;
+  if (e < 0 || e >= p.E) {
+    bad = true;
+    return -1;
+  }
+  const int r = e / p.L;
+  int code = e | (r << 10);
+  if (kRank) {
+    bool first = true;
+    const int64_t t = i / p.K;
+    for (int64_t j = t * p.K; j < i; ++j) {
+      const int e2 = __ldg(p.idx + j);
+      if (e2 >= 0 && e2 < p.E && e2 / p.L == r) first = false;
+    }
+    if (first) code |= kFirstBit;
+  }
+  return code;
+}
+
+template <bool kRank, bool kLL, bool kStaged>
+__global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutParams p) {
+  extern __shared__ int32_t sm[];
+  const int E = p.E, R = p.R, K = p.K;
+  const int C = E + (kRank ? R : 0);
+  const int NT = blockDim.x, W = NT >> 5;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int cta = blockIdx.x, G = gridDim.x;
   const int64_t N = p.N;
   const int64_t t0 = min(N, static_cast<int64_t>(cta) * p.tokens_per_cta);
   const int64_t t1 = min(N, t0 + p.tokens_per_cta);
-  const int64_t a0 = t0 * K, a1 = t1 * K;
-  const int64_t per_warp = ((a1 - a0 + kLayoutWarps * 32 - 1) / (kLayoutWarps * 32)) * 32;
-  const int64_t wa0 = min(a1, a0 + w * per_warp), wa1 = min(a1, wa0 + per_warp);
+  const int64_t a0 = t0 * K;
+  const int n_ent = static_cast<int>((t1 - t0) * K);    // entries of this chunk
+  const int per_warp = ((n_ent + W * 32 - 1) / (W * 32)) * 32;
+  const int wa0 = min(n_ent, w * per_warp), wa1 = min(n_ent, wa0 + per_warp);
 
-  for (int i = tid; i < kLayoutWarps * C; i += kLayoutThreads) hist[i] = 0;
+  const int CP = C | 1;                // odd row stride: conflict-free column access across warps
+  int32_t* hist = sm;                  // [W][CP]: per-warp counts, then running slots
+  int32_t* base = hist + W * CP;       // [C]: this chunk's prefix over earlier chunks
+  int32_t* tot = base + C;             // [C]: totals, then their exclusive scan
+  int32_t* own = tot + C;              // [C]: this chunk's own count
+  int32_t* tmp = own + C;              // [32]
+  const int PS = max(NT, C);
+  int32_t* part = tmp + 32;            // [2][PS]: partial sums over chunks
+  int32_t* scode = part + 2 * PS;      // [tokens_per_cta * K]: entry codes (kStaged)
+
+  bool bad = false;
+  for (int i = tid; i < W * CP; i += NT) hist[i] = 0;
   if (kRank) {
-    for (int64_t i = t0 * R + tid; i < t1 * R; i += kLayoutThreads) {
+    for (int64_t i = t0 * R + tid; i < t1 * R; i += NT) {
       p.mask[i] = 0;
       p.rank_slot[i] = -1;
     }
   }
-  __syncthreads();
-
-  int32_t* my = hist + w * C;
-
-  // Pass 1: per-warp counts.
-  bool bad = false;
-  for (int64_t b = wa0; b < wa1; b += 32) {
-    const int64_t i = b + lane;
-    const bool in = i < wa1;
-    const int e = in ? __ldg(p.idx + i) : -1;
-    const bool valid = in && e >= 0 && e < E;
-    bad |= in && e != -1 && !valid;
-    const unsigned pe = __match_any_sync(0xffffffffu, valid ? e : -2 - lane);
-    if (valid && lane == __ffs(pe) - 1) my[e] += __popc(pe);
+  if (kStaged) {
+    // One coalesced pass over the chunk's indices; each entry's rank is
+    // computed once here, the first-on-rank flags per token after it.
+    for (int li = tid; li < n_ent; li += NT) {
+      const int e = __ldg(p.idx + a0 + li);
+      int code = -1;
+      if (e != -1) {
+        if (e >= 0 && e < E)
+          code = e | (fast_div(e, p.magic_L) << 10);
+        else
+          bad = true;
+      }
+      scode[li] = code;
+    }
+    __syncthreads();
     if (kRank) {
-      const int r = valid ? e / L : -1;
-      bool first = valid;
-      if (valid) {
-        const int64_t t = i / K;
-        for (int64_t j = t * K; j < i; ++j) {
-          const int e2 = __ldg(p.idx + j);
-          if (e2 >= 0 && e2 < E && e2 / L == r) first = false;
+      for (int tl = tid; tl < static_cast<int>(t1 - t0); tl += NT) {
+        int32_t* row = scode + tl * K;
+        for (int k = 0; k < K; ++k) {
+          const int c = row[k];
+          if (c < 0) continue;
+          bool first = true;
+          for (int kk = 0; kk < k; ++kk) {
+            const int c2 = row[kk];
+            if (c2 >= 0 && code_r(c2) == code_r(c)) first = false;
+          }
+          if (first) row[k] = c | kFirstBit;
         }
       }
-      const unsigned pr = __match_any_sync(0xffffffffu, first ? r : -2 - lane);
-      if (first && lane == __ffs(pr) - 1) my[E + r] += __popc(pr);
     }
-    __syncwarp();
+  }
+  __syncthreads();
+
+  int32_t* my = hist + w * CP;
+
+  // Pass 1: per-warp counts (shared-memory atomics: counting needs no order).
+  for (int li = wa0 + lane; li < wa1; li += 32) {
+    const int code = kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad);
+    if (code >= 0) {
+      atomicAdd(&my[code_e(code)], 1);
+      if (kRank && (code & kFirstBit)) atomicAdd(&my[E + code_r(code)], 1);
+    }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(p.status, EP_ST_BAD_INDEX);
   __syncthreads();
 
-  // Per column: exclusive prefix over warps; the chunk's total goes out.
-  for (int col = tid; col < C; col += kLayoutThreads) {
-    int run = 0;
-    for (int ww = 0; ww < kLayoutWarps; ++ww) {
-      const int v = hist[ww * C + col];
-      hist[ww * C + col] = run;
-      run += v;
+  // Per column: exclusive prefix over warps (one warp per column, lane = warp
+  // index, shuffle scan); the chunk's total goes out.
+  for (int col = w; col < C; col += W) {
+    const int v = lane < W ? hist[lane * CP + col] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
-    own[col] = run;
-    p.ws_chunk[static_cast<int64_t>(cta) * C + col] = run;
+    if (lane < W) hist[lane * CP + col] = incl - v;
+    if (lane == 31) {
+      own[col] = incl;
+      p.ws_chunk[static_cast<int64_t>(cta) * C + col] = incl;
+    }
   }
   if (G > 1)
     grid_barrier(p.ws_barrier, static_cast<unsigned>(G), p.status);
   else
     __syncthreads();
 
-  // Prefix over earlier chunks and totals over all chunks.
-  for (int col = tid; col < C; col += kLayoutThreads) {
-    int pre = 0, total = 0;
-    for (int c = 0; c < G; ++c) {
+  // Prefix over earlier chunks and totals over all chunks. P threads share a
+  // column, each summing every P-th chunk with 8 loads in flight.
+  const int P = max(1, min(NT / C, G));
+  for (int j = tid; j < P * C; j += NT) {
+    const int col = j % C, pp = j / C;
+    int pre = 0, total = 0, c = pp;
+    for (; c + 7 * P < G; c += 8 * P) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(p.ws_chunk + static_cast<int64_t>(c + u * P) * C + col);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        pre += (c + u * P < cta) ? v[u] : 0;
+        total += v[u];
+      }
+    }
+    for (; c < G; c += P) {
       const int v = __ldcg(p.ws_chunk + static_cast<int64_t>(c) * C + col);
       pre += (c < cta) ? v : 0;
       total += v;
+    }
+    part[j] = pre;  // j < P * C <= PS
+    part[PS + j] = total;
+  }
+  __syncthreads();
+  for (int col = tid; col < C; col += NT) {
+    int pre = 0, total = 0;
+    for (int pp = 0; pp < P; ++pp) {
+      pre += part[pp * C + col];
+      total += part[PS + pp * C + col];
     }
     base[col] = pre;
     tot[col] = total;
@@ -161,47 +262,39 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
   const int total_e = block_exclusive_scan(tot, E, tmp);
   const int total_r = kRank ? block_exclusive_scan(tot + E, R, tmp) : 0;
   if (cta == 0 && !kLL) {
-    for (int e = tid; e <= E; e += kLayoutThreads) p.expert_off[e] = (e < E) ? tot[e] : total_e;
+    for (int e = tid; e <= E; e += NT) p.expert_off[e] = (e < E) ? tot[e] : total_e;
     if (kRank)
-      for (int r = tid; r <= R; r += kLayoutThreads) p.rank_off[r] = (r < R) ? tot[E + r] : total_r;
+      for (int r = tid; r <= R; r += NT) p.rank_off[r] = (r < R) ? tot[E + r] : total_r;
   }
   if (kLL) {
     // Chunks are source ranks here: (offset << 32) | count of expert e's rows from source `cta`.
-    for (int e = tid; e < E; e += kLayoutThreads)
+    for (int e = tid; e < E; e += NT)
       p.ll_range[static_cast<int64_t>(e) * R + cta] =
           (static_cast<int64_t>(base[e]) << 32) | static_cast<int64_t>(own[e]);
     if (cta == 0 && tid == 0) *p.ll_hdr = p.hdr_value;
   }
   // Running counters: warp prefix + chunk prefix (+ global offset in normal mode).
-  for (int i = tid; i < kLayoutWarps * C; i += kLayoutThreads) {
-    const int col = i % C;
-    hist[i] += base[col] + (kLL ? 0 : tot[col]);
+  for (int col = w; col < C; col += W) {
+    if (lane < W) hist[lane * CP + col] += base[col] + (kLL ? 0 : tot[col]);
   }
   __syncthreads();
 
-  // Pass 2: slots.
-  bool overflow = false;
-  for (int64_t b = wa0; b < wa1; b += 32) {
-    const int64_t i = b + lane;
-    const bool in = i < wa1;
-    const int e = in ? __ldg(p.idx + i) : -1;
-    const bool valid = in && e >= 0 && e < E;
-    const unsigned pe = __match_any_sync(0xffffffffu, valid ? e : -2 - lane);
+  // Pass 2: slots, in (token, slot) order within the warp's range.
+  bool overflow = false, bad2 = false;
+  for (int b = wa0; b < wa1; b += 32) {
+    const int li = b + lane;
+    const bool in = li < wa1;
+    const int code = in ? (kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad2)) : -1;
+    const bool valid = code >= 0;
+    const int e = code_e(code);
+    const unsigned pe = warp_peers(e, valid, p.bits_E);
     const int slot = valid ? my[e] + __popc(pe & lanemask_lt()) : -1;
-    int r = -1, rslot = -1;
-    bool first = false;
+    const bool first = kRank && valid && (code & kFirstBit);
+    const int r = code_r(code);
     unsigned pr = 0;
+    int rslot = -1;
     if (kRank) {
-      r = valid ? e / L : -1;
-      first = valid;
-      if (valid) {
-        const int64_t t = i / K;
-        for (int64_t j = t * K; j < i; ++j) {
-          const int e2 = __ldg(p.idx + j);
-          if (e2 >= 0 && e2 < E && e2 / L == r) first = false;
-        }
-      }
-      pr = __match_any_sync(0xffffffffu, first ? r : -2 - lane);
+      pr = warp_peers(r, first, p.bits_R);
       rslot = first ? my[E + r] + __popc(pr & lanemask_lt()) : -1;
     }
     __syncwarp();
@@ -217,12 +310,13 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
           else
             overflow = true;
         }
-        p.expert_slot[i] = row;
+        p.expert_slot[a0 + li] = row;
       } else {
-        p.expert_slot[i] = slot;
+        p.expert_slot[a0 + li] = slot;
       }
       if (kRank && first) {
-        const int64_t t = i / K;
+        // fast_div is exact below 2^20, which bounds a staged chunk
+        const int64_t t = t0 + (kStaged ? fast_div(li, p.magic_K) : li / K);
         p.rank_slot[t * R + r] = rslot;
         p.mask[t * R + r] = 1;
       }
@@ -231,56 +325,109 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_kernel(const LayoutPara
   if (kLL && __any_sync(0xffffffffu, overflow) && lane == 0) flag(p.status, EP_ST_LL_OVERFLOW);
 }
 
+// ---- host side ---------------------------------------------------------------
+constexpr size_t kMaxStagedEntries = 24576;  // 96 KB of entry codes per CTA
+constexpr int kVariants = 8;                 // kRank x kLL x kStaged
+constexpr int kMaxDevices = 64;
+constexpr size_t kHistBudget = 96 * 1024;    // per-warp counters
+
+// Threads per block: as many warps (up to 32) as the per-warp counters allow.
+static int layout_threads(int E, int R, bool with_rank) {
+  const size_t C = static_cast<size_t>(E) + (with_rank ? R : 0);
+  int W = 32;
+  while (W > 4 && static_cast<size_t>(W) * C * sizeof(int32_t) > kHistBudget) W >>= 1;
+  return W * 32;
+}
+
+static size_t layout_smem(int E, int R, bool with_rank, int threads, size_t staged_entries) {
+  const size_t C = static_cast<size_t>(E) + (with_rank ? R : 0);
+  const size_t CP = C | 1;
+  const size_t W = threads / 32;
+  const size_t PS = C > static_cast<size_t>(threads) ? C : static_cast<size_t>(threads);
+  return sizeof(int32_t) * (W * CP + 3 * C + 32 + 2 * PS + staged_entries);
+}
+
 size_t layout_smem_bytes(int E, int R, bool with_rank) {
-  const int C = E + (with_rank ? R : 0);
-  return sizeof(int32_t) * (static_cast<size_t>(kLayoutWarps) * C + 3 * C + 32);
+  return layout_smem(E, R, with_rank, layout_threads(E, R, with_rank), 0);
 }
 
-template <bool kRank, bool kLL>
-static const void* layout_fn() {
-  return reinterpret_cast<const void*>(&layout_kernel<kRank, kLL>);
+static const void* layout_fn(bool rank, bool ll, bool staged) {
+  const void* fns[kVariants] = {
+      reinterpret_cast<const void*>(&layout_kernel<false, false, false>),
+      reinterpret_cast<const void*>(&layout_kernel<false, false, true>),
+      reinterpret_cast<const void*>(&layout_kernel<false, true, false>),
+      reinterpret_cast<const void*>(&layout_kernel<false, true, true>),
+      reinterpret_cast<const void*>(&layout_kernel<true, false, false>),
+      reinterpret_cast<const void*>(&layout_kernel<true, false, true>),
+      reinterpret_cast<const void*>(&layout_kernel<true, true, false>),
+      reinterpret_cast<const void*>(&layout_kernel<true, true, true>),
+  };
+  return fns[(rank ? 4 : 0) + (ll ? 2 : 0) + (staged ? 1 : 0)];
 }
 
-static const void* pick_layout(bool with_rank, bool ll) {
-  if (ll) return with_rank ? layout_fn<true, true>() : layout_fn<false, true>();
-  return with_rank ? layout_fn<true, false>() : layout_fn<false, false>();
+// Raise each variant's dynamic shared memory limit once per device.
+static bool g_attr_set[kMaxDevices][kVariants];
+
+static cudaError_t prepare(int dev, bool rank, bool ll, bool staged) {
+  const int v = (rank ? 4 : 0) + (ll ? 2 : 0) + (staged ? 1 : 0);
+  if (dev >= 0 && dev < kMaxDevices && g_attr_set[dev][v]) return cudaSuccess;
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const cudaError_t err = cudaFuncSetAttribute(layout_fn(rank, ll, staged),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (err == cudaSuccess && dev >= 0 && dev < kMaxDevices) g_attr_set[dev][v] = true;
+  return err;
+}
+
+static int coresident(int dev, bool rank, bool ll, bool staged, int threads, size_t smem) {
+  int sms = 0, per_sm = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (prepare(dev, rank, ll, staged) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_fn(rank, ll, staged), threads, smem) !=
+      cudaSuccess)
+    return 0;
+  return per_sm * sms;
 }
 
 int layout_max_ctas(int E, int R, bool with_rank) {
-  int dev = 0, sms = 0, coop = 0;
+  int dev = 0, coop = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (!coop) return 0;
-  const size_t smem = layout_smem_bytes(E, R, with_rank);
-  int best = 0;
-  for (int ll = 0; ll < 2; ++ll) {
-    const void* fn = pick_layout(with_rank, ll != 0);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-      return 0;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLayoutThreads, smem) != cudaSuccess)
-      return 0;
-    const int n = per_sm * sms;
-    best = (ll == 0) ? n : (n < best ? n : best);
-  }
-  return best;
+  const int threads = layout_threads(E, R, with_rank);
+  const size_t smem = layout_smem(E, R, with_rank, threads, 0);
+  const int a = coresident(dev, with_rank, false, false, threads, smem);
+  const int b = coresident(dev, with_rank, true, false, threads, smem);
+  return a < b ? a : b;
 }
 
 cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll, cudaStream_t s) {
-  const size_t smem = layout_smem_bytes(p.E, p.R, with_rank);
-  const void* fn = pick_layout(with_rank, ll);
-  cudaError_t err =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int threads = layout_threads(p.E, p.R, with_rank);
+  const size_t entries = static_cast<size_t>(p.tokens_per_cta) * p.K;
+  bool staged = entries <= kMaxStagedEntries;
+  size_t smem = layout_smem(p.E, p.R, with_rank, threads, staged ? entries : 0);
+  if (staged && coresident(dev, with_rank, ll, true, threads, smem) < G) {
+    staged = false;
+    smem = layout_smem(p.E, p.R, with_rank, threads, 0);
+  }
+  err = prepare(dev, with_rank, ll, staged);
   if (err != cudaSuccess) return err;
   if (G > 1) {
     err = cudaMemsetAsync(p.ws_barrier, 0, sizeof(unsigned), s);
     if (err != cudaSuccess) return err;
   }
   LayoutParams q = p;
+  q.magic_L = p.L > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + p.L - 1) / p.L) : 0u;
+  q.magic_K = p.K > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + p.K - 1) / p.K) : 0u;
+  q.bits_E = 0;
+  while ((1 << q.bits_E) < p.E) ++q.bits_E;
+  q.bits_R = 0;
+  while ((1 << q.bits_R) < p.R) ++q.bits_R;
   void* args[] = {&q};
-  return cudaLaunchCooperativeKernel(fn, dim3(G), dim3(kLayoutThreads), args, smem, s);
+  return cudaLaunchCooperativeKernel(layout_fn(with_rank, ll, staged), dim3(G), dim3(threads), args, smem, s);
 }
 
 }  // namespace ep
