@@ -1,10 +1,17 @@
 """Benchmark: MoE layout -> dispatch -> combine on one GB300 (or N replicas).
 
-One step is one pass of the whole hot path over one batch of the large
-prefill workload (16384 tokens, hidden 7168 BF16, 256 experts top-6, 8
-logical ranks): the routing layout, dispatch into the per-rank and the
-expert-major receive buffers (BF16), and combine of identity expert outputs
-(the expert-major rows) back into [16384, 7168] BF16.
+One step is one pass of the whole hot path over one batch of a workload.
+The default workload is the large prefill (16384 tokens, hidden 7168 BF16,
+256 experts top-6, 8 logical ranks): the routing layout, dispatch into the
+per-rank and the expert-major receive buffers (BF16), and combine of
+identity expert outputs (the expert-major rows) back into [16384, 7168] BF16.
+
+--workload 1..5 selects the other synthetic workloads (same JSON line):
+  3, 5  prefill with FP8 dispatch: layout, FP8 dispatch (per-rank and
+        expert-major, E4M3 + per-128-channel scales), combine of BF16 expert
+        outputs (a fixed BF16 buffer in the expert-major layout);
+  1, 2  low latency: send, receive (the hook), combine of BF16 expert outputs
+        in the fixed [E, R*T, H] layout.
 
 Prints one JSON line (rank 0). `value` is tokens/s of the whole job with
 inputs resident in HBM; `e2e` is the same through the C ABI from pinned host
@@ -34,7 +41,7 @@ if ROOT not in sys.path:
 import epinputs as ei  # noqa: E402
 
 METRIC = "dispatch+combine tokens/s and HBM GB/s (% of GB300 peak) at 1 GPU"
-WORKLOAD = 4          # the 16384-token large prefill workload
+DEFAULT_WORKLOAD = 4          # the 16384-token large prefill workload
 L2_FLUSH_BYTES = 256 << 20
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dispatch_kernel_prefill_large.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "combine_ep_get_dispatch_gb300", "csrc", f)
@@ -47,6 +54,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(ei.CONFIGS))
     ap.add_argument("--tokens", type=int, default=None, help="override the token count (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -149,16 +157,166 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
-def algorithmic_bytes(cfg, D_r, D_e):
-    N, H, K, R, E = cfg.N, cfg.H, cfg.K, cfg.R, cfg.E
-    row = H * 2
-    layout = N * K * 4 + (N * K * 4 + N * R * 4 + N * R + 4 * (2 * E + 2 * R + 2))
-    dispatch = (N * row                                   # x read once
-                + N * K * 4 * 3 + N * R * 4               # idx, w, expert_slot, rank_slot read
-                + (D_r + D_e) * row                       # every output row written once
-                + D_e * 4 + D_r * 4 + D_r * K * 8)        # src indices, per-rank top-k idx / weights
-    combine = D_e * row + N * K * 8 + N * row             # rows + slots/weights read, out written
-    return layout, dispatch, combine
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of per-rank timings (every rank gets the result)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens/s: the tokens of all replicas over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
+# ------------------------------------------------------------------ workloads ----
+class NormalWorkload:
+    """Layout, dispatch (per-rank + expert-major, BF16 or FP8), combine."""
+
+    def __init__(self, cfg, dev, inp):
+        import torch
+        import combine_ep_get_dispatch_gb300 as ep
+        self.ep, self.cfg = ep, cfg
+        N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
+        self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
+        self.idx_host = torch.from_numpy(inp["topk_idx"])
+        self.w_host = torch.from_numpy(inp["topk_weights"])
+        self.x, self.idx, self.w = self.x_host.to(dev), self.idx_host.to(dev), self.w_host.to(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # Buffers allocated once (worst-case capacities: no host sync in a step).
+        self.lay = ep.new_layout(self.idx, E, R)
+        self.ws = torch.empty(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device=dev)
+        cap_r, cap_e = N * min(K, R), N * K
+        xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
+        S = H // 128
+        self.rank_x = torch.empty((cap_r, H), dtype=xdt, device=dev)
+        self.rank_s = torch.empty((cap_r, S), dtype=torch.float32, device=dev) if cfg.fp8 else None
+        self.rank_src = torch.empty(cap_r, dtype=torch.int32, device=dev)
+        self.rank_ti = torch.empty((cap_r, K), dtype=torch.int32, device=dev)
+        self.rank_tw = torch.empty((cap_r, K), dtype=torch.float32, device=dev)
+        self.exp_x = torch.empty((cap_e, H), dtype=xdt, device=dev)
+        self.exp_s = torch.empty((cap_e, S), dtype=torch.float32, device=dev) if cfg.fp8 else None
+        self.exp_src = torch.empty(cap_e, dtype=torch.int32, device=dev)
+        self.out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        self.rb = ep._recv_struct(self.rank_x, self.rank_s, self.rank_src, self.rank_ti, self.rank_tw)
+        self.eb = ep._recv_struct(self.exp_x, self.exp_s, self.exp_src)
+        # Expert outputs fed to combine: the BF16 rows themselves (identity
+        # experts) for BF16 dispatch; for FP8 dispatch a BF16 buffer in the
+        # same expert-major layout (what an expert GEMM would write).
+        if cfg.fp8:
+            self.y = torch.empty((cap_e, H), dtype=torch.bfloat16, device=dev)
+            lay0 = ep.get_dispatch_layout(self.idx, E, R)
+            ep.ep_dispatch(lay0, self.x, False, None, None, ep._recv_struct(self.y, None, None))
+        else:
+            self.y = self.exp_x
+        self.phases = ["layout", "dispatch", "combine"]
+        self.dominant = "dispatch"
+        self.kernel_names = {"layout": "layout_kernel", "dispatch": f"dispatch_kernel<{'fp8' if cfg.fp8 else 'bf16'}>",
+                             "combine": "combine_kernel"}
+
+    def layout_for(self, idx):
+        L = self.lay
+        return self.ep.Layout(idx, L.num_experts, L.num_ranks, L.num_tokens_per_rank, L.num_tokens_per_expert,
+                              L.is_token_in_rank, L.rank_offset, L.expert_offset, L.rank_slot, L.expert_slot)
+
+    def run(self, stream, x, idx_layout, w, ev=None):
+        ep = self.ep
+        if ev:
+            ev[0].record(stream)
+        ep.ep_get_dispatch_layout(idx_layout, self.ws, self.status, stream)
+        if ev:
+            ev[1].record(stream)
+        ep.ep_dispatch(idx_layout, x, self.cfg.fp8, w, self.rb, self.eb, self.status, stream)
+        if ev:
+            ev[2].record(stream)
+        ep.ep_combine(idx_layout, self.y, w, self.out, self.status, stream)
+        if ev:
+            ev[3].record(stream)
+
+    def rows(self):
+        return {"per_rank": int(self.lay.rank_offset[-1].item()), "expert_major": int(self.lay.expert_offset[-1].item())}
+
+    def algorithmic_bytes(self):
+        cfg = self.cfg
+        N, H, K, R, E = cfg.N, cfg.H, cfg.K, cfg.R, cfg.E
+        rows = self.rows()
+        D_r, D_e = rows["per_rank"], rows["expert_major"]
+        out_row = H + (H // 128) * 4 if cfg.fp8 else 2 * H
+        layout = N * K * 4 + (N * K * 4 + N * R * 4 + N * R + 4 * (2 * E + 2 * R + 2))
+        dispatch = (N * 2 * H                                 # x read once
+                    + N * K * 4 * 3 + N * R * 4               # idx, w, expert_slot, rank_slot read
+                    + (D_r + D_e) * out_row                   # every output row (and its scales) written once
+                    + D_e * 4 + D_r * 4 + D_r * K * 8)        # src indices, per-rank top-k idx / weights
+        combine = D_e * 2 * H + N * K * 8 + N * 2 * H         # rows + slots/weights read, out written
+        return {"layout": layout, "dispatch": dispatch, "combine": combine}
+
+
+class LLWorkload:
+    """Low-latency send, receive (the hook) and combine on the fixed [E, R*T, H] layout."""
+
+    def __init__(self, cfg, dev, inp):
+        import torch
+        import combine_ep_get_dispatch_gb300 as ep
+        self.ep, self.cfg = ep, cfg
+        N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
+        self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
+        self.idx_host = torch.from_numpy(inp["topk_idx"])
+        self.w_host = torch.from_numpy(inp["topk_weights"])
+        self.x, self.idx, self.w = self.x_host.to(dev), self.idx_host.to(dev), self.w_host.to(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device=dev)
+        xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
+        self.recv_x = torch.empty((E, R * T, H), dtype=xdt, device=dev)
+        self.recv_s = torch.empty((E, R * T, H // 128), dtype=torch.float32, device=dev) if cfg.fp8 else None
+        self.recv_src = torch.empty((E, R * T), dtype=torch.int32, device=dev)
+        self.recv_count = torch.empty(E, dtype=torch.int32, device=dev)
+        self.layout_range = torch.empty((E, R), dtype=torch.int64, device=dev)
+        self.out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        if cfg.fp8:
+            # BF16 expert outputs in the receive layout (what an expert GEMM would write).
+            self.y = torch.empty((E, R * T, H), dtype=torch.bfloat16, device=dev)
+            ep.ep_ll_dispatch_send(self.x, self.idx, H, E, R, T, False, self.y, None, self.recv_src, self.ws)
+        else:
+            self.y = self.recv_x
+        self.phases = ["send", "recv", "combine"]
+        self.dominant = "send"
+        self.kernel_names = {"send": "layout_kernel<ll> + dispatch_kernel", "recv": "ll_recv_kernel",
+                             "combine": "combine_kernel"}
+
+    def layout_for(self, idx):
+        return idx
+
+    def run(self, stream, x, idx, w, ev=None):
+        ep, c = self.ep, self.cfg
+        if ev:
+            ev[0].record(stream)
+        ep.ep_ll_dispatch_send(x, idx, c.H, c.E, c.R, c.T, c.fp8, self.recv_x, self.recv_s, self.recv_src,
+                               self.ws, self.status, stream)
+        if ev:
+            ev[1].record(stream)
+        ep.ep_ll_dispatch_recv(self.ws, c.N, c.K, c.E, c.R, c.T, self.recv_count, self.layout_range,
+                               self.status, stream)
+        if ev:
+            ev[2].record(stream)
+        ep.ep_ll_combine(self.y, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status, stream)
+        if ev:
+            ev[3].record(stream)
+
+    def rows(self):
+        return {"received": int(self.recv_count.sum().item())}
+
+    def algorithmic_bytes(self):
+        c = self.cfg
+        N, H, K, R, E = c.N, c.H, c.K, c.R, c.E
+        D = self.rows()["received"]
+        row = H + (H // 128) * 4 if c.fp8 else 2 * H
+        send = N * 2 * H + N * K * 4 + D * row + D * 4 + N * K * 4 + E * R * 8 + E * 4
+        recv = 2 * (E * 4 + E * R * 8)
+        combine = D * 2 * H + N * K * 8 + N * 2 * H
+        return {"send": send, "recv": recv, "combine": combine}
 
 
 def run_ours(args):
@@ -171,131 +329,100 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    cfg = ei.CONFIGS[WORKLOAD]
+    cfg = ei.CONFIGS[args.workload]
     if args.tokens:
         cfg = cfg.scaled(N=args.tokens)
-    N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
     inp = ei.make_inputs(cfg, seed=0)
-    x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
-    idx_host = torch.from_numpy(inp["topk_idx"])
-    w_host = torch.from_numpy(inp["topk_weights"])
-    x = x_host.to(dev)
-    idx = idx_host.to(dev)
-    w = w_host.to(dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    wl = (LLWorkload if cfg.mode == "ll" else NormalWorkload)(cfg, dev, inp)
     stream = torch.cuda.current_stream(dev)
-
-    # Buffers allocated once (worst-case capacities: no host sync in a step).
-    lay = ep.new_layout(idx, E, R)
-    ws = torch.empty(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device=dev)
-    cap_r, cap_e = N * min(K, R), N * K
-    rank_x = torch.empty((cap_r, H), dtype=torch.bfloat16, device=dev)
-    rank_src = torch.empty(cap_r, dtype=torch.int32, device=dev)
-    rank_ti = torch.empty((cap_r, K), dtype=torch.int32, device=dev)
-    rank_tw = torch.empty((cap_r, K), dtype=torch.float32, device=dev)
-    exp_x = torch.empty((cap_e, H), dtype=torch.bfloat16, device=dev)
-    exp_src = torch.empty(cap_e, dtype=torch.int32, device=dev)
-    out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-    rb = ep._recv_struct(rank_x, None, rank_src, rank_ti, rank_tw)
-    eb = ep._recv_struct(exp_x, None, exp_src)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    def layout_for(idxi):
-        # Same output arrays, a different topk_idx buffer.
-        return ep.Layout(idxi, E, R, lay.num_tokens_per_rank, lay.num_tokens_per_expert, lay.is_token_in_rank,
-                         lay.rank_offset, lay.expert_offset, lay.rank_slot, lay.expert_slot)
-
-    def step(li, xi, wi, ev=None):
-        if ev:
-            ev[0].record(stream)
-        ep.ep_get_dispatch_layout(li, ws, status, stream)
-        if ev:
-            ev[1].record(stream)
-        ep.ep_dispatch(li, xi, False, wi, rb, eb, status, stream)
-        if ev:
-            ev[2].record(stream)
-        ep.ep_combine(li, exp_x, wi, out, status, stream)
-        if ev:
-            ev[3].record(stream)
+    lay = wl.layout_for(wl.idx)
 
     sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
     time.sleep(0.3)
     for _ in range(args.warmup):
         flush.fill_(1)
-        step(lay, x, w)
+        wl.run(stream, wl.x, lay, wl.w)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    nph = len(wl.phases)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     sampler.mark(True)
     for i in range(args.steps):
         flush.fill_(i & 0xFF)   # write 256 MiB between steps: nothing of the last step stays in L2
-        step(lay, x, w, evs[i])
+        wl.run(stream, wl.x, lay, wl.w, evs[i])
     torch.cuda.synchronize()
     sampler.mark(False)
     if world > 1:
         torch.distributed.barrier()
-    lay_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
-    dis_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
-    com_ms = np.array([e[2].elapsed_time(e[3]) for e in evs])
-    step_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+    phase_ms = {ph: np.array([e[j].elapsed_time(e[j + 1]) for e in evs]) for j, ph in enumerate(wl.phases)}
+    step_ms = np.array([e[0].elapsed_time(e[nph]) for e in evs])
     total_ms = float(step_ms.sum())
-    st = int(status.item())
+    st = int(wl.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {ep.ep_error_string(st)}")
-
-    D_r = int(lay.rank_offset[-1].item())
-    D_e = int(lay.expert_offset[-1].item())
 
     # End to end through the C ABI from pinned host memory.
     e2e = None
     if not args.no_e2e:
-        xp, ip, wp = x_host.pin_memory(), idx_host.pin_memory(), w_host.pin_memory()
-        outp = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
-        xd, idd, wd = torch.empty_like(x), torch.empty_like(idx), torch.empty_like(w)
-        lay_d = layout_for(idd)
+        xp, ip, wp = wl.x_host.pin_memory(), wl.idx_host.pin_memory(), wl.w_host.pin_memory()
+        outp = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
+        xd, idd, wd = torch.empty_like(wl.x), torch.empty_like(wl.idx), torch.empty_like(wl.w)
+        lay_d = wl.layout_for(idd)
         e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            xd.copy_(xp, non_blocking=True)
+            idd.copy_(ip, non_blocking=True)
+            wd.copy_(wp, non_blocking=True)
+            wl.run(stream, xd, lay_d, wd)
+            outp.copy_(wl.out, non_blocking=True)
+
         for _ in range(2):
-            xd.copy_(xp, non_blocking=True); idd.copy_(ip, non_blocking=True); wd.copy_(wp, non_blocking=True)
-            step(lay_d, xd, wd)
-            outp.copy_(out, non_blocking=True)
+            e2e_step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            xd.copy_(xp, non_blocking=True); idd.copy_(ip, non_blocking=True); wd.copy_(wp, non_blocking=True)
-            step(lay_d, xd, wd)
-            outp.copy_(out, non_blocking=True)
+            e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if not torch.equal(outp, out.cpu()):
+        if not torch.equal(outp, wl.out.cpu()):
             raise RuntimeError("e2e output differs from the device-resident run")
         e2e = (e2e_ms, xp.numel() * 2 + ip.numel() * 4 + wp.numel() * 4, outp.numel() * 2)
     sampler.stop()
 
-    # max over ranks
-    times = torch.tensor([total_ms, e2e[0] if e2e else 0.0], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    total_ms, e2e_ms_max = float(times[0]), float(times[1])
+    total_ms, e2e_ms_max = max_over_ranks([total_ms, e2e[0] if e2e else 0.0], dev, world)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
 
     peak, peak_kind = peaks()
-    b_lay, b_dis, b_com = algorithmic_bytes(cfg, D_r, D_e)
-    dis_s, com_s, lay_s = dis_ms.mean() / 1e3, com_ms.mean() / 1e3, lay_ms.mean() / 1e3
+    nbytes = wl.algorithmic_bytes()
+    mean_s = {ph: float(v.mean()) / 1e3 for ph, v in phase_ms.items()}
     ms_per_step = total_ms / args.steps
-    value = N * world / (ms_per_step / 1e3)
-    traffic_full, src_hash = profile_traffic()
+    N = cfg.N
+    value = job_throughput(N, world, ms_per_step)
+    phases = {}
+    for ph in wl.phases:
+        gbs = nbytes[ph] / mean_s[ph] / 1e9
+        phases[f"{ph}_us"] = round(mean_s[ph] * 1e6, 2)
+        phases[f"{ph}_gbs"] = round(gbs, 1)
+        phases[f"{ph}_frac"] = round(gbs / peak, 4)
+    phases["step_gbs"] = round(sum(nbytes.values()) / (ms_per_step / 1e3) / 1e9, 1)
+    phases["peak_note"] = f"fractions of the {peak_kind} HBM copy peak {peak} GB/s"
+    dom = wl.dominant
+    achieved = nbytes[dom] / mean_s[dom] / 1e9
     traffic = None
-    if traffic_full is not None and src_hash == kernel_hash():
-        traffic = traffic_full * (N / ei.CONFIGS[WORKLOAD].N)
-    clocks = sampler.summary()
+    if dom == "dispatch" and not cfg.fp8 and args.workload == DEFAULT_WORKLOAD:
+        traffic_full, src_hash = profile_traffic()
+        if traffic_full is not None and src_hash == kernel_hash():
+            traffic = traffic_full * (N / ei.CONFIGS[DEFAULT_WORKLOAD].N)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -308,31 +435,24 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded: x ~ N(0,1) BF16, router logits N(0,1), softmax top-6 renormalised)",
-        "config": {"workload": cfg.name, "tokens": N, "hidden": H, "experts": E, "topk": K, "ranks": R,
-                   "dispatch_dtype": "bf16", "combine_dtype": "bf16 (fp32 accumulation)",
-                   "l2": "flushed between steps (256 MiB write); inputs and outputs larger than L2",
+        "data": "synthetic (seeded: x ~ N(0,1) BF16, router logits N(0,1) softmax top-k renormalised; "
+                "see epinputs for the grouped and Zipf recipes)",
+        "config": {"workload": cfg.name, "tokens": N, "hidden": cfg.H, "experts": cfg.E, "topk": cfg.K,
+                   "ranks": cfg.R, "max_tokens_per_rank": cfg.T,
+                   "dispatch_dtype": "fp8_e4m3 + fp32 scales / 128 ch" if cfg.fp8 else "bf16",
+                   "combine_dtype": "bf16 (fp32 accumulation)",
+                   "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "rows": {"per_rank": D_r, "expert_major": D_e}},
-        "phases": {
-            "layout_us": round(lay_s * 1e6, 2),
-            "dispatch_us": round(dis_s * 1e6, 2),
-            "combine_us": round(com_s * 1e6, 2),
-            "dispatch_gbs": round(b_dis / dis_s / 1e9, 1),
-            "combine_gbs": round(b_com / com_s / 1e9, 1),
-            "dispatch_frac": round(b_dis / dis_s / 1e9 / peak, 4),
-            "combine_frac": round(b_com / com_s / 1e9 / peak, 4),
-            "step_gbs": round((b_lay + b_dis + b_com) / (ms_per_step / 1e3) / 1e9, 1),
-            "peak_note": f"fractions of the {peak_kind} HBM copy peak {peak} GB/s",
-        },
-        "roofline": {"bound": "hbm", "kernel": "dispatch_kernel<bf16>", "achieved": round(b_dis / dis_s / 1e9, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(b_dis / dis_s / 1e9 / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": b_dis, "peak_kind": peak_kind},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
+                   "rows": wl.rows()},
+        "phases": phases,
+        "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind},
+        "gpu_launches": (3 if cfg.mode != "ll" else 4) * args.steps,
+        "clocks": sampler.summary(),
     }
     if e2e:
-        line["e2e"] = {"value": round(N * world / (e2e_ms_max / 1e3), 1), "unit": "tokens/s",
+        line["e2e"] = {"value": round(job_throughput(N, world, e2e_ms_max), 1), "unit": "tokens/s",
                        "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
                        "ms_per_step": round(e2e_ms_max, 4)}
     if world == 1 and not args.no_cpu_baseline:
@@ -342,22 +462,36 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# --------------------------------------------------------------- CPU oracle ----
 def _oracle_step(sub):
     import oracle
+    if sub["mode"] == "ll":
+        ll = oracle.ll_dispatch(sub["x"], sub["topk_idx"], sub["E"], sub["R"], sub["T"], sub["fp8"])
+        y = ll["recv_x"] if not sub["fp8"] else np.zeros(ll["recv_x"].shape, np.uint16)
+        oracle.ll_combine(y, ll["slot_map"], sub["topk_weights"])
+        return
     lay = oracle.layout(sub["topk_idx"], sub["E"], sub["R"])
-    o = oracle.dispatch(sub["x"], sub["topk_idx"], sub["topk_weights"], sub["E"], sub["R"], False, lay=lay)
-    oracle.combine(o["exp_x"], lay["expert_slot"], sub["topk_weights"])
+    o = oracle.dispatch(sub["x"], sub["topk_idx"], sub["topk_weights"], sub["E"], sub["R"], sub["fp8"], lay=lay)
+    y = o["exp_x"] if not sub["fp8"] else o["exp_x"].astype(np.uint16)
+    oracle.combine(y, lay["expert_slot"], sub["topk_weights"])
 
 
 def _sample(cfg, n_tok):
+    if cfg.mode == "ll":
+        n_tok = max(cfg.R, (min(n_tok, cfg.N) // cfg.R) * cfg.R)
+    else:
+        n_tok = min(n_tok, cfg.N)
     d = ei.make_inputs(cfg.scaled(N=n_tok), seed=0)
-    d.update(E=cfg.E, R=cfg.R)
+    # Low latency: the sample's own per-rank capacity (rows do not depend on T).
+    T = max(1, n_tok // cfg.R) if cfg.mode == "ll" else None
+    d.update(E=cfg.E, R=cfg.R, T=T, fp8=cfg.fp8, mode=cfg.mode, n_tok=n_tok)
     return d
 
 
 def cpu_baseline(cfg, n_tok):
     """The oracle as written (single thread) on the first n_tok tokens of the workload."""
     sub = _sample(cfg, n_tok)
+    n_tok = sub["n_tok"]
     _oracle_step(sub)  # warm the library and the page cache
     reps, t = 0, 0.0
     while t < 10.0 and reps < 20:
@@ -366,7 +500,7 @@ def cpu_baseline(cfg, n_tok):
         t += time.perf_counter() - t0
         reps += 1
     return {"value": round(n_tok * reps / t, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_tok} of {cfg.N} tokens of {cfg.name} (layout + BF16 dispatch + combine), "
+            "sample": f"{n_tok} of {cfg.N} tokens of {cfg.name} (the whole step on those tokens), "
                       f"{reps} reps, {t:.1f} s"}
 
 
@@ -374,9 +508,9 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    cfg = ei.CONFIGS[WORKLOAD]
-    n_tok = 256
-    sub = _sample(cfg, n_tok)
+    cfg = ei.CONFIGS[args.workload]
+    sub = _sample(cfg, 256)
+    n_tok = sub["n_tok"]
     for _ in range(args.warmup):
         _oracle_step(sub)
     t0 = time.perf_counter()

@@ -8,7 +8,7 @@
 // over unmasked slots, in slot order, one fp32 fused multiply-add per term.
 //
 // Design (HBM-bound, read-heavy: K rows read, one row written per token).
-// One block per token (grid-stride). The token's slots and weights go to
+// One block per token. The token's slots and weights go to
 // shared memory once; each thread then owns 16-byte vectors of the row and,
 // for up to 8 slots at a time, issues all their loads before the FMAs, so K
 // independent 16-byte reads per thread are in flight. The reduction happens
@@ -107,11 +107,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t full = static_cast<int64_t>(sms) * 16;
-  const int grid = static_cast<int>(p.N < full ? p.N : full);
+  // One block per token: the hardware scheduler hands blocks to SMs as
+  // they free up.
+  const int64_t cap = int64_t(1) << 30;
+  const int grid = static_cast<int>(p.N < cap ? p.N : cap);
   combine_kernel<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

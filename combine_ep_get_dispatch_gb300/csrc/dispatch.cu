@@ -11,16 +11,16 @@
 //                   nearest), q = e4m3_rn_satfinite(x / s_b); s_b = 0 -> q = e4m3(x)
 //
 // Design (HBM-bound, write-heavy: one row read, ~R'+K' rows written).
-// Each warp owns a token at a time and a two-stage shared-memory row buffer.
-// Lane 0 brings the next token's BF16 row in with one bulk TMA copy
+// BF16: each warp owns a token at a time and a two-stage shared-memory row
+// buffer. Lane 0 brings the next token's row in with one bulk TMA copy
 // (cp.async.bulk global->shared, completion on an mbarrier) while the current
-// row is written out. For FP8 the warp quantises the staged row in shared
-// memory (half a warp per 128-channel block, shuffle max, IEEE division,
-// cvt.rn.satfinite.e4m3x2) into a second two-stage buffer. Every destination
-// row is then one bulk TMA store (cp.async.bulk shared->global) issued by the
-// lane that owns that destination: the copy engine generates the addresses,
-// the SM issues ~R'+K' instructions per token. Grid: persistent, a multiple
-// of the SM count.
+// row is written out; every destination row is one bulk TMA store
+// (cp.async.bulk shared->global) issued by the lane that owns that
+// destination, so the copy engine generates the addresses and the SM issues
+// ~R'+K' instructions per token. Grid: persistent, a multiple of the SM count.
+// FP8: a register path (see dispatch_fp8_kernel below): quantisation needs
+// the SM anyway, and without the BF16 staging buffers five times more warps
+// fit on an SM.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -31,86 +31,33 @@ namespace {
 constexpr int kMaxWarps = 4;
 
 struct WarpSmem {
-  unsigned row_bf16;   // bytes of one staged BF16 row (2H)
-  unsigned row_q;      // bytes of one quantised row (H), FP8 only
-  unsigned row_s;      // bytes of one scale row (H/128 * 4, rounded to 16), FP8 only
-  unsigned per_warp;   // total bytes per warp, 128-aligned
+  unsigned row_bf16;   // bytes of one staged BF16 row (2H, rounded to 128)
+  unsigned per_warp;   // total bytes per warp (two stages)
 };
 
 __host__ __device__ inline unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline WarpSmem warp_smem(int H, bool fp8) {
+__host__ __device__ inline WarpSmem warp_smem(int H) {
   WarpSmem w;
   w.row_bf16 = round_up(static_cast<unsigned>(H) * 2u, 128u);
-  w.row_q = fp8 ? round_up(static_cast<unsigned>(H), 128u) : 0u;
-  w.row_s = fp8 ? round_up(static_cast<unsigned>(H / 128) * 4u, 128u) : 0u;
-  w.per_warp = 2u * (w.row_bf16 + w.row_q + w.row_s);
+  w.per_warp = 2u * w.row_bf16;
   return w;
 }
 
 constexpr unsigned kBarBytes = 128;  // 2 mbarriers per warp, up to 8 warps
 
-// Quantise one staged BF16 row (H channels) into E4M3 codes and fp32 scales.
-// Half a warp per 128-channel block: lane j of the half holds channels
-// [8j, 8j+8) of the block.
-__device__ __forceinline__ void quantize_row_smem(const uint8_t* src, uint8_t* q, float* sc, int H,
-                                                  int lane) {
-  const int half = lane >> 4, j = lane & 15;
-  const int nblk = H / 128;
-  // Warp-uniform trip count: both halves run every iteration (the shuffles
-  // name the whole warp); a half past the last block only idles.
-  for (int b0 = 0; b0 < nblk; b0 += 2) {
-    const int b = b0 + half;
-    const bool active = b < nblk;
-    float f[8];
-    if (active) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + b * 256 + j * 16);
-      f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-      f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-      f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-      f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = 0.0f;
-    }
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (!active) continue;
-    const float s = __fdiv_rn(m, 448.0f);
-    if (s > 0.0f) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = __fdiv_rn(f[i], s);
-    }
-    uint2 out;
-    out.x = pack_e4m3x2(f[0], f[1]) | (pack_e4m3x2(f[2], f[3]) << 16);
-    out.y = pack_e4m3x2(f[4], f[5]) | (pack_e4m3x2(f[6], f[7]) << 16);
-    *reinterpret_cast<uint2*>(q + b * 128 + j * 8) = out;
-    if (j == 0) sc[b] = s;
-  }
-}
-
-template <bool kFP8>
-__global__ void __launch_bounds__(kMaxWarps * 32) dispatch_kernel(const DispatchParams p) {
+__global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const DispatchParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, W = blockDim.x >> 5;
   const int H = p.H, K = p.K, R = p.R, L = p.L, E = p.E;
-  const WarpSmem ws = warp_smem(H, kFP8);
+  const WarpSmem ws = warp_smem(H);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + 2 * w;
   uint8_t* wb = smem + kBarBytes + static_cast<size_t>(w) * ws.per_warp;
-  // Stage s of each buffer: BF16 row at wb + s*rb, E4M3 row at qbase + s*rq,
-  // scales at sbase + s*rs.
-  const unsigned rb = ws.row_bf16, rq = ws.row_q, rs = ws.row_s;
-  uint8_t* const qbase = wb + 2 * rb;
-  uint8_t* const sbase = wb + 2 * rb + 2 * rq;
+  // Stage s: the BF16 row at wb + s * rb.
+  const unsigned rb = ws.row_bf16;
 
   const unsigned xbytes = static_cast<unsigned>(H) * 2u;
-  const unsigned obytes = kFP8 ? static_cast<unsigned>(H) : xbytes;
-  const unsigned sbytes = static_cast<unsigned>(H / 128) * 4u;
-  const bool scale_bulk = kFP8 && (sbytes % 16u == 0u);
-  const int64_t nsc = H / 128;
+  const unsigned obytes = xbytes;
 
   if (lane == 0) {
     mbar_init(&bar[0], 1);
@@ -134,10 +81,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_kernel(const Dispatch
     const int s = it & 1;
     const int64_t tn = t + nw;
     if (tn < N) {
-      if (kFP8)
-        fence_proxy_async_smem();  // quantisation reads of stage s^1 precede the refill
-      else
-        bulk_wait_read<0>();       // the stores of the previous token read stage s^1
+      bulk_wait_read<0>();  // the stores of the previous token read stage s^1
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar[s ^ 1], xbytes);
@@ -169,29 +113,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_kernel(const Dispatch
     pending &= ~(1u << s);
 
     const uint8_t* src = wb + s * rb;
-    const float* scl = nullptr;
-    if (kFP8) {
-      bulk_wait_read<1>();  // the stores of two tokens ago read E4M3 row and scales s
-      __syncwarp();
-      uint8_t* qs = qbase + s * rq;
-      float* ss = reinterpret_cast<float*>(sbase + s * rs);
-      quantize_row_smem(wb + s * rb, qs, ss, H, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      src = qs;
-      scl = ss;
-    }
 
     // Expert-major copies.
-    if (erow >= 0) {
-      bulk_s2g(p.exp_x + static_cast<int64_t>(erow) * obytes, src, obytes);
-      if (kFP8 && p.exp_scales) {
-        if (scale_bulk)
-          bulk_s2g(p.exp_scales + static_cast<int64_t>(erow) * nsc, scl, sbytes);
-        else
-          for (int64_t b = 0; b < nsc; ++b) p.exp_scales[erow * nsc + b] = scl[b];
-      }
-    }
+    if (erow >= 0) bulk_s2g(p.exp_x + static_cast<int64_t>(erow) * obytes, src, obytes);
 
     // Per-rank copies: lane owns ranks lane, lane + 32, ...
     if (p.rank_x) {
@@ -204,12 +128,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_kernel(const Dispatch
         }
         if (rrow >= 0) {
           bulk_s2g(p.rank_x + static_cast<int64_t>(rrow) * obytes, src, obytes);
-          if (kFP8 && p.rank_scales) {
-            if (scale_bulk)
-              bulk_s2g(p.rank_scales + static_cast<int64_t>(rrow) * nsc, scl, sbytes);
-            else
-              for (int64_t b = 0; b < nsc; ++b) p.rank_scales[rrow * nsc + b] = scl[b];
-          }
           if (p.rank_src) p.rank_src[rrow] = static_cast<int32_t>(t);
         }
         if (p.rank_topk_idx || p.rank_topk_w) {
@@ -234,15 +152,162 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_kernel(const Dispatch
   bulk_wait<0>();
 }
 
-template <bool kFP8>
-cudaError_t launch_impl(const DispatchParams& p, cudaStream_t s) {
+// ---- FP8 dispatch: register path ---------------------------------------------
+// A warp per token. Lanes own 16 consecutive channels of a 512-channel step
+// (8 lanes = one 128-channel block): two 16-byte loads of BF16, a shuffle max
+// over the block, the IEEE division by the scale, 16 E4M3 codes packed into
+// one 16-byte store per destination row. Shared memory holds only the
+// token's destination list and its scales, so up to 40 warps share an SM and
+// hide the quantisation latency. (Measured against staging the E4M3 row in
+// shared memory and writing it with bulk TMA stores, which was slower here.)
+constexpr int kF8Threads = 256;
+constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank copies
+
+struct F8Warp {
+  uint8_t* xdst[kF8MaxDest];
+  float* sdst[kF8MaxDest];
+  float scales[EP_MAX_HIDDEN / 128];
+};
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
+}
+
+__global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const DispatchParams p) {
+  __shared__ F8Warp sw[kF8Threads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  F8Warp& me = sw[w];
+  const int H = p.H, K = p.K, R = p.R, L = p.L, E = p.E;
+  const int64_t nsc = H / 128;
+  const int64_t N = p.N;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + w; t < N; t += nw) {
+    // Destinations: expert-major rows (lane k < K), then per-rank rows.
+    int e_k = -1;
+    float w_k = 0.0f;
+    int32_t erow = -1;
+    if (lane < K) {
+      e_k = __ldg(p.idx + t * K + lane);
+      if (p.w) w_k = __ldg(p.w + t * K + lane);
+      if (p.exp_x) {
+        erow = __ldg(p.expert_slot + t * K + lane);
+        if (erow >= p.exp_cap) {
+          flag(p.status, p.overflow_bit);
+          erow = -1;
+        }
+        if (erow >= 0 && p.exp_src)
+          p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
+      }
+    }
+    const unsigned vm = __ballot_sync(0xffffffffu, erow >= 0);
+    if (erow >= 0) {
+      const int pos = __popc(vm & lanemask_lt());
+      me.xdst[pos] = p.exp_x + static_cast<int64_t>(erow) * H;
+      me.sdst[pos] = p.exp_scales ? p.exp_scales + static_cast<int64_t>(erow) * nsc : nullptr;
+    }
+    int n = __popc(vm);
+    if (p.rank_x) {
+      for (int rb = 0; rb < R; rb += 32) {
+        const int r = rb + lane;
+        int32_t rrow = (r < R) ? __ldg(p.rank_slot + t * R + r) : -1;
+        if (rrow >= p.rank_cap) {
+          flag(p.status, EP_ST_CAPACITY);
+          rrow = -1;
+        }
+        const unsigned rm = __ballot_sync(0xffffffffu, rrow >= 0);
+        // at most K ranks hold a copy of one token; the list has room for K more
+        if (rrow >= 0) {
+          const int pos = n + __popc(rm & lanemask_lt());
+          if (pos < kF8MaxDest) {
+            me.xdst[pos] = p.rank_x + static_cast<int64_t>(rrow) * H;
+            me.sdst[pos] = p.rank_scales ? p.rank_scales + static_cast<int64_t>(rrow) * nsc : nullptr;
+          }
+          if (p.rank_src) p.rank_src[rrow] = static_cast<int32_t>(t);
+        }
+        n = min(n + __popc(rm), kF8MaxDest);
+        if (p.rank_topk_idx || p.rank_topk_w) {
+          for (int kk = 0; kk < K; ++kk) {
+            const int ek = __shfl_sync(0xffffffffu, e_k, kk);
+            const float wk = __shfl_sync(0xffffffffu, w_k, kk);
+            if (rrow >= 0) {
+              const bool here = ek >= 0 && ek < E && ek / L == r;
+              if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? ek - r * L : -1;
+              if (p.rank_topk_w) p.rank_topk_w[static_cast<int64_t>(rrow) * K + kk] = here ? wk : 0.0f;
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+
+    // Quantise and store, 512 channels per step.
+    const uint16_t* xr = p.x + t * H;
+    for (int c0 = 0; c0 < H; c0 += 512) {
+      const int c = c0 + lane * 16;
+      const bool act = c < H;
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (act) {
+        v0 = __ldg(reinterpret_cast<const uint4*>(xr + c));
+        v1 = __ldg(reinterpret_cast<const uint4*>(xr + c + 8));
+      }
+      float f[16];
+      f[0] = bf16_lo(v0.x); f[1] = bf16_hi(v0.x); f[2] = bf16_lo(v0.y); f[3] = bf16_hi(v0.y);
+      f[4] = bf16_lo(v0.z); f[5] = bf16_hi(v0.z); f[6] = bf16_lo(v0.w); f[7] = bf16_hi(v0.w);
+      f[8] = bf16_lo(v1.x); f[9] = bf16_hi(v1.x); f[10] = bf16_lo(v1.y); f[11] = bf16_hi(v1.y);
+      f[12] = bf16_lo(v1.z); f[13] = bf16_hi(v1.z); f[14] = bf16_lo(v1.w); f[15] = bf16_hi(v1.w);
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const float sc = __fdiv_rn(m, 448.0f);
+      if (sc > 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
+      }
+      uint4 q;
+      q.x = e4m3x4(f[0], f[1], f[2], f[3]);
+      q.y = e4m3x4(f[4], f[5], f[6], f[7]);
+      q.z = e4m3x4(f[8], f[9], f[10], f[11]);
+      q.w = e4m3x4(f[12], f[13], f[14], f[15]);
+      if (act && (lane & 7) == 0) me.scales[c >> 7] = sc;
+      if (act)
+        for (int d = 0; d < n; ++d) st_v4(me.xdst[d] + c, q);
+    }
+    __syncwarp();
+    for (int d = 0; d < n; ++d) {
+      float* sd = me.sdst[d];
+      if (sd)
+        for (int64_t b = lane; b < nsc; b += 32) sd[b] = me.scales[b];
+    }
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
-  const WarpSmem ws = warp_smem(p.H, kFP8);
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel, kF8Threads, 0);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int wpb = kF8Threads / 32;
+  const int64_t need = (p.N + wpb - 1) / wpb;
+  const int64_t full = static_cast<int64_t>(per_sm) * sms;
+  dispatch_fp8_kernel<<<static_cast<int>(need < full ? need : full), kF8Threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s) {
+  if (p.N <= 0) return cudaSuccess;
+  const WarpSmem ws = warp_smem(p.H);
   int W = kMaxWarps;
   const unsigned budget = 200u * 1024u;
   while (W > 1 && kBarBytes + W * ws.per_warp > budget) --W;
   const size_t smem = kBarBytes + static_cast<size_t>(W) * ws.per_warp;
-  const void* fn = reinterpret_cast<const void*>(&dispatch_kernel<kFP8>);
+  const void* fn = reinterpret_cast<const void*>(&dispatch_bf16_kernel);
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0, per_sm = 0;
@@ -254,14 +319,14 @@ cudaError_t launch_impl(const DispatchParams& p, cudaStream_t s) {
   const int64_t need = (p.N + W - 1) / W;
   const int64_t full = static_cast<int64_t>(per_sm) * sms;
   const int grid = static_cast<int>(need < full ? need : full);
-  dispatch_kernel<kFP8><<<grid, W * 32, smem, s>>>(p);
+  dispatch_bf16_kernel<<<grid, W * 32, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchParams& p, bool fp8, cudaStream_t s) {
-  return fp8 ? launch_impl<true>(p, s) : launch_impl<false>(p, s);
+  return fp8 ? launch_fp8(p, s) : launch_bf16(p, s);
 }
 
 }  // namespace ep
