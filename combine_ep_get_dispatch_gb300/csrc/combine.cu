@@ -38,7 +38,10 @@ __device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b)
   return a.N == b.N && a.K == b.K && a.E == b.E && a.R == b.R && a.T == b.T;
 }
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+// Block b handles token b / nchunk and the b % nchunk-th of nchunk equal
+// spans of its row (nchunk > 1 only when there are few tokens: it spreads a
+// small batch over more SMs).
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int nchunk) {
   __shared__ int32_t s_row[EP_MAX_TOPK];
   __shared__ float s_w[EP_MAX_TOPK];
   __shared__ int s_ok;
@@ -60,7 +63,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     if (!s_ok) return;
   }
   const int nvec = H / 8;
-  for (int64_t t = blockIdx.x; t < p.N; t += gridDim.x) {
+  const int span = (nvec + nchunk - 1) / nchunk;
+  const int64_t items = static_cast<int64_t>(p.N) * nchunk;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t t = it / nchunk;
+    const int v0 = static_cast<int>(it - t * nchunk) * span;
+    const int v1 = min(nvec, v0 + span);
     if (tid < K) {
       int32_t row = __ldg(p.slot + t * K + tid);
       if (row >= p.y_rows) {
@@ -72,7 +80,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     }
     __syncthreads();
     uint16_t* out = p.out + t * H;
-    for (int v = tid; v < nvec; v += kThreads) {
+    for (int v = v0 + tid; v < v1; v += kThreads) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -107,11 +115,25 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
-  // One block per token: the hardware scheduler hands blocks to SMs as
-  // they free up.
+  // One block per token (the hardware scheduler hands blocks to SMs as they
+  // free up); a batch with fewer tokens than eight blocks per SM splits each
+  // row into up to nvec / 128 spans.
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int nvec = p.H / 8;
+  int nchunk = 1;
+  const int64_t want = static_cast<int64_t>(sms) * 8;
+  if (p.N < want) {
+    nchunk = static_cast<int>((want + p.N - 1) / p.N);
+    const int most = (nvec + kThreads - 1) / kThreads;
+    if (nchunk > most) nchunk = most;
+    if (nchunk < 1) nchunk = 1;
+  }
+  const int64_t items = static_cast<int64_t>(p.N) * nchunk;
   const int64_t cap = int64_t(1) << 30;
-  const int grid = static_cast<int>(p.N < cap ? p.N : cap);
-  combine_kernel<<<grid, kThreads, 0, s>>>(p);
+  const int grid = static_cast<int>(items < cap ? items : cap);
+  combine_kernel<<<grid, kThreads, 0, s>>>(p, nchunk);
   return cudaGetLastError();
 }
 

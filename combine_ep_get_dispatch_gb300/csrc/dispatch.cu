@@ -173,6 +173,33 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
 }
 
+// 16 BF16 channels of one lane -> 16 E4M3 codes; the 8 lanes of a 128-channel
+// block share the block's scale s = amax / 448 (all 32 lanes must call it).
+__device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, float& sc) {
+  float f[16];
+  f[0] = bf16_lo(v0.x); f[1] = bf16_hi(v0.x); f[2] = bf16_lo(v0.y); f[3] = bf16_hi(v0.y);
+  f[4] = bf16_lo(v0.z); f[5] = bf16_hi(v0.z); f[6] = bf16_lo(v0.w); f[7] = bf16_hi(v0.w);
+  f[8] = bf16_lo(v1.x); f[9] = bf16_hi(v1.x); f[10] = bf16_lo(v1.y); f[11] = bf16_hi(v1.y);
+  f[12] = bf16_lo(v1.z); f[13] = bf16_hi(v1.z); f[14] = bf16_lo(v1.w); f[15] = bf16_hi(v1.w);
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  sc = __fdiv_rn(m, 448.0f);
+  if (sc > 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
+  }
+  uint4 q;
+  q.x = e4m3x4(f[0], f[1], f[2], f[3]);
+  q.y = e4m3x4(f[4], f[5], f[6], f[7]);
+  q.z = e4m3x4(f[8], f[9], f[10], f[11]);
+  q.w = e4m3x4(f[12], f[13], f[14], f[15]);
+  return q;
+}
+
 __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const DispatchParams p) {
   __shared__ F8Warp sw[kF8Threads / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -240,40 +267,23 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
     }
     __syncwarp();
 
-    // Quantise and store, 512 channels per step.
+    // Quantise and store, 512 channels per step. (Loading several steps
+    // ahead was measured: the extra registers cost more warps than the
+    // deeper loads gained.)
     const uint16_t* xr = p.x + t * H;
     for (int c0 = 0; c0 < H; c0 += 512) {
       const int c = c0 + lane * 16;
-      const bool act = c < H;
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (act) {
+      if (c < H) {
         v0 = __ldg(reinterpret_cast<const uint4*>(xr + c));
         v1 = __ldg(reinterpret_cast<const uint4*>(xr + c + 8));
       }
-      float f[16];
-      f[0] = bf16_lo(v0.x); f[1] = bf16_hi(v0.x); f[2] = bf16_lo(v0.y); f[3] = bf16_hi(v0.y);
-      f[4] = bf16_lo(v0.z); f[5] = bf16_hi(v0.z); f[6] = bf16_lo(v0.w); f[7] = bf16_hi(v0.w);
-      f[8] = bf16_lo(v1.x); f[9] = bf16_hi(v1.x); f[10] = bf16_lo(v1.y); f[11] = bf16_hi(v1.y);
-      f[12] = bf16_lo(v1.z); f[13] = bf16_hi(v1.z); f[14] = bf16_lo(v1.w); f[15] = bf16_hi(v1.w);
-      float m = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      const float sc = __fdiv_rn(m, 448.0f);
-      if (sc > 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
-      }
-      uint4 q;
-      q.x = e4m3x4(f[0], f[1], f[2], f[3]);
-      q.y = e4m3x4(f[4], f[5], f[6], f[7]);
-      q.z = e4m3x4(f[8], f[9], f[10], f[11]);
-      q.w = e4m3x4(f[12], f[13], f[14], f[15]);
-      if (act && (lane & 7) == 0) me.scales[c >> 7] = sc;
-      if (act)
+      float sc;
+      const uint4 q = quantize16(v0, v1, sc);
+      if (c < H) {
+        if ((lane & 7) == 0) me.scales[c >> 7] = sc;
         for (int d = 0; d < n; ++d) st_v4(me.xdst[d] + c, q);
+      }
     }
     __syncwarp();
     for (int d = 0; d < n; ++d) {
@@ -303,16 +313,19 @@ cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s) {
 cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
   const WarpSmem ws = warp_smem(p.H);
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Up to 4 warps per CTA; a batch with fewer tokens than 4 per SM uses
+  // fewer, so its rows spread over more SMs (and their copy engines).
   int W = kMaxWarps;
+  while (W > 1 && static_cast<int64_t>(W) * sms > p.N * 2) W >>= 1;
   const unsigned budget = 200u * 1024u;
   while (W > 1 && kBarBytes + W * ws.per_warp > budget) --W;
   const size_t smem = kBarBytes + static_cast<size_t>(W) * ws.per_warp;
   const void* fn = reinterpret_cast<const void*>(&dispatch_bf16_kernel);
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, W * 32, smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
