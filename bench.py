@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(ei.CONFIGS))
     ap.add_argument("--tokens", type=int, default=None, help="override the token count (profiling runs)")
+    ap.add_argument("--ll-combine", default="one-phase", choices=["one-phase", "two-phase"],
+                    help="low-latency workloads: combine in one launch, or send + receive hook")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
@@ -257,7 +259,7 @@ class NormalWorkload:
 class LLWorkload:
     """Low-latency send, receive (the hook) and combine on the fixed [E, R*T, H] layout."""
 
-    def __init__(self, cfg, dev, inp):
+    def __init__(self, cfg, dev, inp, two_phase=False):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
@@ -281,10 +283,16 @@ class LLWorkload:
             ep.ep_ll_dispatch_send(self.x, self.idx, H, E, R, T, False, self.y, None, self.recv_src, self.ws)
         else:
             self.y = self.recv_x
-        self.phases = ["send", "recv", "combine"]
+        self.two_phase = two_phase
+        if two_phase:
+            self.staging = torch.empty((N * K, H), dtype=torch.bfloat16, device=dev)
+            self.phases = ["send", "recv", "combine_send", "combine_recv"]
+        else:
+            self.phases = ["send", "recv", "combine"]
         self.dominant = "send"
         self.kernel_names = {"send": "layout_kernel<ll> + dispatch_kernel", "recv": "ll_recv_kernel",
-                             "combine": "combine_kernel"}
+                             "combine": "combine_kernel", "combine_send": "combine_kernel<gather>",
+                             "combine_recv": "combine_kernel"}
 
     def layout_for(self, idx):
         return idx
@@ -301,6 +309,15 @@ class LLWorkload:
                                self.status, stream)
         if ev:
             ev[2].record(stream)
+        if self.two_phase:
+            ep.ep_ll_combine_send(self.y, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.staging, self.status, stream)
+            if ev:
+                ev[3].record(stream)
+            ep.ep_ll_combine_recv(self.staging, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status,
+                                  stream)
+            if ev:
+                ev[4].record(stream)
+            return
         ep.ep_ll_combine(self.y, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status, stream)
         if ev:
             ev[3].record(stream)
@@ -316,6 +333,9 @@ class LLWorkload:
         send = N * 2 * H + N * K * 4 + D * row + D * 4 + N * K * 4 + E * R * 8 + E * 4
         recv = 2 * (E * 4 + E * R * 8)
         combine = D * 2 * H + N * K * 8 + N * 2 * H
+        if self.two_phase:
+            return {"send": send, "recv": recv, "combine_send": D * 2 * H * 2 + N * K * 4,
+                    "combine_recv": D * 2 * H + N * K * 8 + N * 2 * H}
         return {"send": send, "recv": recv, "combine": combine}
 
 
@@ -333,7 +353,10 @@ def run_ours(args):
     if args.tokens:
         cfg = cfg.scaled(N=args.tokens)
     inp = ei.make_inputs(cfg, seed=0)
-    wl = (LLWorkload if cfg.mode == "ll" else NormalWorkload)(cfg, dev, inp)
+    if cfg.mode == "ll":
+        wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase")
+    else:
+        wl = NormalWorkload(cfg, dev, inp)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lay = wl.layout_for(wl.idx)
@@ -448,7 +471,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind},
-        "gpu_launches": (3 if cfg.mode != "ll" else 4) * args.steps,
+        "gpu_launches": (3 if cfg.mode != "ll" else 3 + len(wl.phases) - 2) * args.steps,
         "clocks": sampler.summary(),
     }
     if e2e:

@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         "ep_ll_dispatch_recv": (I, [P, SZ, I, I, I, I, I, P, P, P, P]),
         "ep_ll_combine": (I, [P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_fp8_e4m3_encode": (I, [P, P, I64, P]),
+        "ep_ll_combine_send": (I, [P, P, SZ, I, I, I, I, I, I, P, P, P]),
+        "ep_ll_combine_recv": (I, [P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -244,6 +246,17 @@ def ep_ll_combine(expert_y, topk_weights, workspace, N, K, H, E, R, T, out, stat
                   stream=None) -> None:
     _check(lib().ep_ll_combine(_p(expert_y), _p(topk_weights), _p(workspace), workspace.numel(), N, K, H,
                                E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine")
+
+
+def ep_ll_combine_send(expert_y, workspace, N, K, H, E, R, T, staging, status=None, stream=None) -> None:
+    _check(lib().ep_ll_combine_send(_p(expert_y), _p(workspace), workspace.numel(), N, K, H, E, R, T,
+                                    _p(staging), _p(status), _stream(stream)), "ep_ll_combine_send")
+
+
+def ep_ll_combine_recv(staging, topk_weights, workspace, N, K, H, E, R, T, out, status=None,
+                       stream=None) -> None:
+    _check(lib().ep_ll_combine_recv(_p(staging), _p(topk_weights), _p(workspace), workspace.numel(), N, K, H,
+                                    E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine_recv")
 
 
 def ep_fp8_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
@@ -392,11 +405,26 @@ def low_latency_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, num_max_dispat
 
 def low_latency_combine(expert_y: torch.Tensor, topk_weights: torch.Tensor, handle: LLHandle,
                         out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                        stream=None) -> torch.Tensor:
-    """out [N, H] bf16 from expert outputs in the [E, R*T, H] receive layout."""
+                        return_recv_hook: bool = False, stream=None):
+    """out [N, H] bf16 from expert outputs in the [E, R*T, H] receive layout.
+
+    return_recv_hook=False: one launch, returns out. True: the send phase
+    gathers the rows back into a token-major staging buffer now and the
+    returned hook runs the weighted sum; returns (out, hook), out valid after
+    hook() ("DeepEP V1 (legacy) guide", section 6.1).
+    """
     h = handle
     if out is None:
         out = torch.empty((h.N, h.H), dtype=torch.bfloat16, device=expert_y.device)
-    ep_ll_combine(expert_y.contiguous(), topk_weights.contiguous(), h.workspace, h.N, h.K, h.H, h.E, h.R, h.T,
-                  out, status, stream)
-    return out
+    y = expert_y.contiguous()
+    w = topk_weights.contiguous()
+    if not return_recv_hook:
+        ep_ll_combine(y, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream)
+        return out
+    staging = torch.empty((h.N * h.K, h.H), dtype=torch.bfloat16, device=y.device)
+    ep_ll_combine_send(y, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, staging, status, stream)
+
+    def hook() -> None:
+        ep_ll_combine_recv(staging, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream)
+
+    return out, hook

@@ -305,6 +305,54 @@ int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* w
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
 
+int ep_ll_combine_send(const void* expert_y, const void* workspace, size_t workspace_bytes, int N, int K, int H,
+                       int E, int R, int T, void* staging, int32_t* status, void* stream) {
+  int rc = ll_common_checks(N, K, E, R, T);
+  if (rc != EP_OK) return rc;
+  if (!hidden_ok(H, 0)) return EP_ERR_INVALID_ARG;
+  if (!expert_y || (N > 0 && !staging)) return EP_ERR_INVALID_ARG;
+  if (!aligned16(expert_y) || !aligned16(staging)) return EP_ERR_ALIGNMENT;
+  const LLWs w = ll_ws(N, K, E, R);
+  if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  void* ws = const_cast<void*>(workspace);
+  CombineParams p{};
+  p.y = static_cast<const uint16_t*>(expert_y);
+  p.y_rows = static_cast<int64_t>(E) * R * T;
+  p.slot = at<int32_t>(ws, w.slot);
+  p.out = static_cast<uint16_t*>(staging);
+  p.N = N; p.K = K; p.H = H;
+  p.gather = 1;
+  p.ll_hdr = at<LLHeader>(ws, w.hdr);
+  p.ll_expect = LLHeader{kMagicSent, N, K, E, R, T, H, 0, 0};
+  p.status = status;
+  return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_ll_combine_recv(const void* staging, const float* topk_weights, const void* workspace,
+                       size_t workspace_bytes, int N, int K, int H, int E, int R, int T, void* out,
+                       int32_t* status, void* stream) {
+  int rc = ll_common_checks(N, K, E, R, T);
+  if (rc != EP_OK) return rc;
+  if (!hidden_ok(H, 0)) return EP_ERR_INVALID_ARG;
+  if (N > 0 && (!staging || !topk_weights || !out)) return EP_ERR_INVALID_ARG;
+  if (!aligned16(staging) || !aligned16(out)) return EP_ERR_ALIGNMENT;
+  const LLWs w = ll_ws(N, K, E, R);
+  if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  void* ws = const_cast<void*>(workspace);
+  CombineParams p{};
+  p.y = static_cast<const uint16_t*>(staging);
+  p.y_rows = static_cast<int64_t>(N) * K;
+  p.slot = at<int32_t>(ws, w.slot);
+  p.token_major = 1;
+  p.w = topk_weights;
+  p.out = static_cast<uint16_t*>(out);
+  p.N = N; p.K = K; p.H = H;
+  p.ll_hdr = at<LLHeader>(ws, w.hdr);
+  p.ll_expect = LLHeader{kMagicSent, N, K, E, R, T, H, 0, 0};
+  p.status = status;
+  return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
 int ep_fp8_e4m3_encode(const float* in, uint8_t* out, int64_t n, void* stream) {
   if (n < 0 || (n > 0 && (!in || !out))) return EP_ERR_INVALID_ARG;
   return cuda_rc(launch_e4m3_encode(in, out, n, static_cast<cudaStream_t>(stream)));

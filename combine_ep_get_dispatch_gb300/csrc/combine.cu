@@ -40,7 +40,10 @@ __device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b)
 
 // Block b handles token b / nchunk and the b % nchunk-th of nchunk equal
 // spans of its row (nchunk > 1 only when there are few tokens: it spreads a
-// small batch over more SMs).
+// small batch over more SMs). kGather copies each routed row to its own
+// output row t*K + k instead of summing (the send half of the two-phase
+// low-latency combine).
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int nchunk) {
   __shared__ int32_t s_row[EP_MAX_TOPK];
   __shared__ float s_w[EP_MAX_TOPK];
@@ -71,15 +74,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int v1 = min(nvec, v0 + span);
     if (tid < K) {
       int32_t row = __ldg(p.slot + t * K + tid);
+      if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + tid);
       if (row >= p.y_rows) {
         flag(p.status, EP_ST_CAPACITY);
         row = -1;
       }
       s_row[tid] = row;
-      s_w[tid] = __ldg(p.w + t * K + tid);
+      s_w[tid] = p.w ? __ldg(p.w + t * K + tid) : 1.0f;
     }
     __syncthreads();
-    uint16_t* out = p.out + t * H;
     for (int v = v0 + tid; v < v1; v += kThreads) {
       float acc[8];
 #pragma unroll
@@ -97,15 +100,27 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
         for (int j = 0; j < kChunk; ++j) {
           const int k = k0 + j;
           const int32_t row = (k < K) ? s_row[k] : -1;
-          if (row >= 0) fma8(acc, s_w[k], yv[j]);
+          if (row < 0) continue;
+          if (kGather)
+            reinterpret_cast<uint4*>(p.out + (t * K + k) * H)[v] = yv[j];
+          else
+            fma8(acc, s_w[k], yv[j]);
         }
+      }
+      if (kGather) continue;
+      if (p.bias) {
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.bias + t * H) + v);
+        acc[0] += bf16_lo(b.x); acc[1] += bf16_hi(b.x);
+        acc[2] += bf16_lo(b.y); acc[3] += bf16_hi(b.y);
+        acc[4] += bf16_lo(b.z); acc[5] += bf16_hi(b.z);
+        acc[6] += bf16_lo(b.w); acc[7] += bf16_hi(b.w);
       }
       uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);
       o.y = pack_bf16x2(acc[2], acc[3]);
       o.z = pack_bf16x2(acc[4], acc[5]);
       o.w = pack_bf16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(out)[v] = o;
+      reinterpret_cast<uint4*>(p.out + t * H)[v] = o;
     }
     __syncthreads();
   }
@@ -133,7 +148,10 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(p.N) * nchunk;
   const int64_t cap = int64_t(1) << 30;
   const int grid = static_cast<int>(items < cap ? items : cap);
-  combine_kernel<<<grid, kThreads, 0, s>>>(p, nchunk);
+  if (p.gather)
+    combine_kernel<true><<<grid, kThreads, 0, s>>>(p, nchunk);
+  else
+    combine_kernel<false><<<grid, kThreads, 0, s>>>(p, nchunk);
   return cudaGetLastError();
 }
 

@@ -67,10 +67,13 @@ struct DispatchParams {
 struct CombineParams {
   const uint16_t* y;     // [y_rows, H] BF16
   int64_t y_rows;
-  const int32_t* slot;   // [N, K]
-  const float* w;        // [N, K]
-  uint16_t* out;         // [N, H]
+  const int32_t* slot;   // [N, K] rows of y, -1 = masked
+  const float* w;        // [N, K]; null: every weight is 1
+  const uint16_t* bias;  // [N, H] BF16 added after the weighted sum, or null
+  uint16_t* out;         // [N, H]; gather mode: [N * K, H]
   int N, K, H;
+  int token_major;       // read row t*K + k (for slot >= 0) instead of the slot value
+  int gather;            // copy every routed row to out[t*K + k] instead of summing
   const LLHeader* ll_hdr;  // low-latency: the send's header (null in normal mode)
   LLHeader ll_expect;
   int32_t* status;

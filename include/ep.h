@@ -306,6 +306,42 @@ int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* w
                   int32_t* status, void* stream);
 
 /*
+ * Two-phase low-latency combine, send phase: the expert outputs go back to
+ * their source tokens ("DeepEP V1 (legacy) guide", section 6.1:
+ * low_latency_combine also returns a receive hook; "How DeepEP enables
+ * hook-based overlapping", "Two-Phase Kernel Architecture"). On one GPU the
+ * "transfer" gathers every routed row y[e][j(t, k)] into the token-major
+ * staging row t * K + k; masked slots are not written.
+ *
+ *   expert_y   [E, R*T, hidden] BF16 expert outputs in the receive layout
+ *   workspace  filled by the send of this batch (same sizes)
+ *   staging    [N * K, hidden] BF16, caller-owned
+ *   status     EP_ST_NOT_SENT / EP_ST_MISMATCH as for ep_ll_combine
+ * The result of send followed by receive equals ep_ll_combine bit for bit
+ * (same values, same fp32 fused multiply-add chain); the single-phase call
+ * moves fewer bytes, the two-phase form lets other work run in between.
+ */
+int ep_ll_combine_send(const void* expert_y, const void* workspace, size_t workspace_bytes,
+                       int num_tokens, int num_topk, int hidden, int num_experts, int num_ranks,
+                       int max_tokens_per_rank, void* staging, int32_t* status, void* stream);
+
+/*
+ * Two-phase low-latency combine, receive phase (the hook): out[t] =
+ * bf16( sum over unmasked k in slot order of w[t, k] * staging[t * K + k] ),
+ * the same fp32 fused multiply-add chain as ep_combine.
+ *
+ *   staging       [N * K, hidden] BF16 written by ep_ll_combine_send
+ *   topk_weights  [N, K] fp32
+ *   workspace     the same workspace (it says which slots are masked)
+ *   out           [N, hidden] BF16
+ * Must be ordered after the send phase on the stream.
+ */
+int ep_ll_combine_recv(const void* staging, const float* topk_weights, const void* workspace,
+                       size_t workspace_bytes, int num_tokens, int num_topk, int hidden,
+                       int num_experts, int num_ranks, int max_tokens_per_rank, void* out,
+                       int32_t* status, void* stream);
+
+/*
  * Element-wise fp32 -> FP8 E4M3 conversion (round to nearest even, saturated
  * to +-448, NaN -> NaN), the encoder the FP8 dispatch applies to x / s
  * (DeepEP V1 guide section 5.2(6)). n >= 0 elements; in and out device

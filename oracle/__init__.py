@@ -56,6 +56,10 @@ def lib():
         L.oracle_ll_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32,
                                          P, P, P, P, P, P]
         L.oracle_ll_dispatch.restype = i32
+        L.oracle_gather_rows.argtypes = [P, i64, P, i32, i32, i32, P]
+        L.oracle_gather_rows.restype = i32
+        L.oracle_combine_staged.argtypes = [P, P, P, i32, i32, i32, P]
+        L.oracle_combine_staged.restype = i32
         _lib = L
     return _lib
 
@@ -204,3 +208,26 @@ def ll_dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, E: int, R: int, T: int
 def ll_combine(y_bf16: np.ndarray, slot_map: np.ndarray, topk_weights: np.ndarray) -> tuple:
     """Low-latency combine: y is [E, R*T, H]; slot_map rows index its flattened view."""
     return combine(y_bf16.reshape(-1, y_bf16.shape[-1]), slot_map, topk_weights)
+
+
+def ll_combine_send(y_bf16: np.ndarray, slot_map: np.ndarray) -> tuple:
+    """Token-major staging [N*K, H]: row t*K + k is y's row slot_map[t, k] (unwritten rows stay 0)."""
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16).reshape(-1, y_bf16.shape[-1])
+    slot = np.ascontiguousarray(slot_map, dtype=np.int32)
+    N, K = slot.shape
+    H = y.shape[1]
+    staging = np.zeros((N * K, H), np.uint16)
+    st = lib().oracle_gather_rows(_p(y), y.shape[0], _p(slot), N, K, H, _p(staging))
+    return staging, int(st)
+
+
+def ll_combine_recv(staging: np.ndarray, slot_map: np.ndarray, topk_weights: np.ndarray) -> np.ndarray:
+    """Weighted sum of the staged rows of every routed slot."""
+    st_ = np.ascontiguousarray(staging, dtype=np.uint16)
+    slot = np.ascontiguousarray(slot_map, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    N, K = slot.shape
+    H = st_.shape[1]
+    out = np.empty((N, H), np.uint16)
+    lib().oracle_combine_staged(_p(st_), _p(slot), _p(w), N, K, H, _p(out))
+    return out

@@ -291,6 +291,41 @@ int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const
   return status;
 }
 
+// Two-phase low-latency combine, send half: the output row of every routed
+// (token, slot) is copied back to the token-major staging row t*K + k.
+int oracle_gather_rows(const uint16_t* y, int64_t y_rows, const int32_t* slot, int N, int K, int H,
+                       uint16_t* staging) {
+  int status = 0;
+  for (int t = 0; t < N; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int64_t tk = static_cast<int64_t>(t) * K + k;
+      const int32_t row = slot[tk];
+      if (row < 0) continue;
+      if (row >= y_rows) { status |= kCapacity; continue; }
+      std::memcpy(staging + tk * H, y + static_cast<int64_t>(row) * H, sizeof(uint16_t) * H);
+    }
+  return status;
+}
+
+// Two-phase low-latency combine, receive half: the weighted sum of the
+// staged rows t*K + k over the slots the send did route (slot[t,k] >= 0), in
+// slot order, one fused multiply-add per term, BF16 at the end.
+int oracle_combine_staged(const uint16_t* staging, const int32_t* slot, const float* w, int N, int K, int H,
+                          uint16_t* out) {
+  std::vector<float> acc(H);
+  for (int t = 0; t < N; ++t) {
+    std::fill(acc.begin(), acc.end(), 0.0f);
+    for (int k = 0; k < K; ++k) {
+      const int64_t tk = static_cast<int64_t>(t) * K + k;
+      if (slot[tk] < 0) continue;
+      const float wk = w[tk];
+      for (int h = 0; h < H; ++h) acc[h] = std::fmaf(wk, f32_from_bf16(staging[tk * H + h]), acc[h]);
+    }
+    for (int h = 0; h < H; ++h) out[static_cast<int64_t>(t) * H + h] = bf16_from_f32(acc[h]);
+  }
+  return 0;
+}
+
 // Low-latency dispatch. Tokens are split contiguously over R source ranks,
 // n_s = N / R each (n_s <= T). The receive buffer of expert e is the fixed
 // region [e][0 .. R*T) of recv_x [E, R*T, H]; the rank owning e sees it as

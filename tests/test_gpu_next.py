@@ -1,0 +1,139 @@
+"""GPU parity of the rows built after the hot path: the two-phase low-latency
+combine and CUDA-graph capture of the low-latency and the normal paths."""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_get_dispatch_gb300 as ep
+import epinputs as ei
+import oracle
+from helpers import status_value, to_dev, to_dev_bf16, u16, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _expert_outputs(shape, seed):
+    n = int(np.prod(shape))
+    z = ei.normal(ei.stream_key(seed, 600), n).astype(np.float32) * 2.0
+    return ei.bf16_bits_from_f32(z).reshape(shape)
+
+
+@pytest.mark.parametrize("c,n_s,H", [(1, 16, 7168), (2, 16, 1024)])
+def test_two_phase_ll_combine(c, n_s, H):
+    cfg = ei.CONFIGS[c].scaled(N=ei.CONFIGS[c].R * n_s, H=H)
+    d = ei.make_inputs(cfg, seed=c + 20)
+    st = _status()
+    recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), cfg.T, cfg.E,
+                                                      cfg.R, use_fp8=cfg.fp8, status=st)
+    hook()
+    ref = oracle.ll_dispatch(d["x"], d["topk_idx"], cfg.E, cfg.R, cfg.T, False)
+    y = _expert_outputs((cfg.E, cfg.R * cfg.T, H), seed=c)
+    w = to_dev(d["topk_weights"])
+    out, chook = ep.low_latency_combine(to_dev_bf16(y), w, handle, status=st, return_recv_hook=True)
+    chook()
+    one = ep.low_latency_combine(to_dev_bf16(y), w, handle, status=st)
+    want = oracle.ll_combine_recv(oracle.ll_combine_send(y, ref["slot_map"])[0], ref["slot_map"],
+                                  d["topk_weights"])
+    assert np.array_equal(u16(out), want)
+    assert np.array_equal(u16(one), want)
+    assert status_value(st) == 0
+
+
+def test_ll_path_in_a_cuda_graph():
+    """send + receive + combine captured once, replayed on two batches."""
+    cfg = ei.CONFIGS[1].scaled(H=2048)
+    N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
+    x = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device="cuda")
+    recv_x = torch.empty((E, R * T, H), dtype=torch.bfloat16, device="cuda")
+    recv_src = torch.empty((E, R * T), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(E, dtype=torch.int32, device="cuda")
+    rng = torch.empty((E, R), dtype=torch.int64, device="cuda")
+    out = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    st = _status()
+
+    def step():
+        ep.ep_ll_dispatch_send(x, idx, H, E, R, T, False, recv_x, None, recv_src, ws, st)
+        ep.ep_ll_dispatch_recv(ws, N, K, E, R, T, cnt, rng, st)
+        ep.ep_ll_combine(recv_x, w, ws, N, K, H, E, R, T, out, st)
+
+    d0 = ei.make_inputs(cfg, seed=30)
+    x.copy_(to_dev_bf16(d0["x"])); idx.copy_(to_dev(d0["topk_idx"])); w.copy_(to_dev(d0["topk_weights"]))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (31, 32):
+        d = ei.make_inputs(cfg, seed=seed)
+        x.copy_(to_dev_bf16(d["x"])); idx.copy_(to_dev(d["topk_idx"])); w.copy_(to_dev(d["topk_weights"]))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.ll_dispatch(d["x"], d["topk_idx"], E, R, T, False)
+        assert np.array_equal(cnt.cpu().numpy(), ref["recv_count"])
+        ref_out, _ = oracle.ll_combine(ref["recv_x"], ref["slot_map"], d["topk_weights"])
+        assert np.array_equal(u16(out), ref_out)
+    assert status_value(st) == 0
+
+
+def test_normal_path_in_a_cuda_graph():
+    """layout + dispatch (worst-case capacities) + combine captured once, replayed on two batches."""
+    cfg = ei.CONFIGS[3].scaled(N=512, H=1024)
+    N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
+    x = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    lay = ep.new_layout(idx, E, R)
+    ws = torch.empty(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device="cuda")
+    ex = torch.empty((N * K, H), dtype=torch.uint8, device="cuda")
+    es = torch.empty((N * K, H // 128), dtype=torch.float32, device="cuda")
+    ysrc = torch.empty((N * K, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    st = _status()
+
+    def step():
+        ep.ep_get_dispatch_layout(lay, ws, st)
+        ep.ep_dispatch(lay, x, True, w, None, ep._recv_struct(ex, es, None), st)
+        ep.ep_dispatch(lay, x, False, w, None, ep._recv_struct(ysrc, None, None), st)
+        ep.ep_combine(lay, ysrc, w, out, st)
+
+    d0 = ei.make_inputs(cfg, seed=40)
+    x.copy_(to_dev_bf16(d0["x"])); idx.copy_(to_dev(d0["topk_idx"])); w.copy_(to_dev(d0["topk_weights"]))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (41, 42):
+        d = ei.make_inputs(cfg, seed=seed)
+        x.copy_(to_dev_bf16(d["x"])); idx.copy_(to_dev(d["topk_idx"])); w.copy_(to_dev(d["topk_weights"]))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.dispatch(d["x"], d["topk_idx"], d["topk_weights"], E, R, True, with_rank=False)
+        D_e = ref["exp_x"].shape[0]
+        assert np.array_equal(u8(ex[:D_e]), ref["exp_x"])
+        assert np.array_equal(es[:D_e].cpu().numpy(), ref["exp_scales"])
+        ref_out, _ = oracle.combine(u16(ysrc[:D_e]), ref["layout"]["expert_slot"], d["topk_weights"])
+        assert np.array_equal(u16(out), ref_out)
+        assert np.array_equal(lay.expert_slot.cpu().numpy(), ref["layout"]["expert_slot"])
+    assert status_value(st) == 0

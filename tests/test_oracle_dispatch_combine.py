@@ -238,3 +238,23 @@ def test_ll_overflow_flagged():
     x, idx, w = _inputs(cfg)
     ll = oracle.ll_dispatch(x, idx, cfg.E, cfg.R, 16, False)
     assert ll["status"] & oracle.LL_OVERFLOW
+
+
+def test_two_phase_ll_combine_equals_single_phase():
+    # Send half: every routed (t, k) row lands at staging row t*K + k, a copy
+    # of y's row; receive half: the same weighted sum as the one-launch combine
+    # ("DeepEP V1 guide" 6.1: low_latency_combine with a receive hook).
+    cfg = ei.CONFIGS[2].scaled(N=32 * 8, H=256)
+    x, idx, w = _inputs(cfg, seed=4)
+    ll = oracle.ll_dispatch(x, idx, cfg.E, cfg.R, cfg.T, False)
+    y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(9, 3), ll["recv_x"].size).astype(np.float32))
+    y = y.reshape(ll["recv_x"].shape)
+    staging, st = oracle.ll_combine_send(y, ll["slot_map"])
+    assert st == 0
+    sm = ll["slot_map"].reshape(-1)
+    ok = sm >= 0
+    assert np.array_equal(staging[ok], y.reshape(-1, cfg.H)[sm[ok]])
+    assert np.all(staging[~ok] == 0)
+    two = oracle.ll_combine_recv(staging, ll["slot_map"], w)
+    one, _ = oracle.ll_combine(y, ll["slot_map"], w)
+    assert np.array_equal(two, one)
