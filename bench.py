@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(ei.CONFIGS))
     ap.add_argument("--tokens", type=int, default=None, help="override the token count (profiling runs)")
+    ap.add_argument("--fp8-scales", default="fp32", choices=["fp32", "pow2", "ue8m0"],
+                    help="FP8 workloads: fp32 scales, power-of-two fp32 scales, or UE8M0 bytes")
     ap.add_argument("--ll-combine", default="one-phase", choices=["one-phase", "two-phase"],
                     help="low-latency workloads: combine in one launch, or send + receive hook")
     ap.add_argument("--no-e2e", action="store_true")
@@ -175,13 +177,19 @@ def job_throughput(tokens_per_rank, world, ms_per_step):
 
 
 # ------------------------------------------------------------------ workloads ----
+def fp8_flag_word(ep, cfg, scales: str) -> int:
+    return ep.fp8_flags(cfg.fp8, round_scale=scales == "pow2", use_ue8m0=scales == "ue8m0")
+
+
 class NormalWorkload:
     """Layout, dispatch (per-rank + expert-major, BF16 or FP8), combine."""
 
-    def __init__(self, cfg, dev, inp):
+    def __init__(self, cfg, dev, inp, scales="fp32"):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
+        self.flags = fp8_flag_word(ep, cfg, scales)
+        sdt = torch.uint8 if scales == "ue8m0" else torch.float32
         N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
         self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
         self.idx_host = torch.from_numpy(inp["topk_idx"])
@@ -195,12 +203,12 @@ class NormalWorkload:
         xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
         S = H // 128
         self.rank_x = torch.empty((cap_r, H), dtype=xdt, device=dev)
-        self.rank_s = torch.empty((cap_r, S), dtype=torch.float32, device=dev) if cfg.fp8 else None
+        self.rank_s = torch.empty((cap_r, S), dtype=sdt, device=dev) if cfg.fp8 else None
         self.rank_src = torch.empty(cap_r, dtype=torch.int32, device=dev)
         self.rank_ti = torch.empty((cap_r, K), dtype=torch.int32, device=dev)
         self.rank_tw = torch.empty((cap_r, K), dtype=torch.float32, device=dev)
         self.exp_x = torch.empty((cap_e, H), dtype=xdt, device=dev)
-        self.exp_s = torch.empty((cap_e, S), dtype=torch.float32, device=dev) if cfg.fp8 else None
+        self.exp_s = torch.empty((cap_e, S), dtype=sdt, device=dev) if cfg.fp8 else None
         self.exp_src = torch.empty(cap_e, dtype=torch.int32, device=dev)
         self.out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
         self.rb = ep._recv_struct(self.rank_x, self.rank_s, self.rank_src, self.rank_ti, self.rank_tw)
@@ -231,7 +239,7 @@ class NormalWorkload:
         ep.ep_get_dispatch_layout(idx_layout, self.ws, self.status, stream)
         if ev:
             ev[1].record(stream)
-        ep.ep_dispatch(idx_layout, x, self.cfg.fp8, w, self.rb, self.eb, self.status, stream)
+        ep.ep_dispatch(idx_layout, x, self.flags, w, self.rb, self.eb, self.status, stream)
         if ev:
             ev[2].record(stream)
         ep.ep_combine(idx_layout, self.y, w, self.out, self.status, stream)
@@ -246,7 +254,7 @@ class NormalWorkload:
         N, H, K, R, E = cfg.N, cfg.H, cfg.K, cfg.R, cfg.E
         rows = self.rows()
         D_r, D_e = rows["per_rank"], rows["expert_major"]
-        out_row = H + (H // 128) * 4 if cfg.fp8 else 2 * H
+        out_row = H + (H // 128) * self.rank_s.element_size() if cfg.fp8 else 2 * H
         layout = N * K * 4 + (N * K * 4 + N * R * 4 + N * R + 4 * (2 * E + 2 * R + 2))
         dispatch = (N * 2 * H                                 # x read once
                     + N * K * 4 * 3 + N * R * 4               # idx, w, expert_slot, rank_slot read
@@ -259,10 +267,12 @@ class NormalWorkload:
 class LLWorkload:
     """Low-latency send, receive (the hook) and combine on the fixed [E, R*T, H] layout."""
 
-    def __init__(self, cfg, dev, inp, two_phase=False):
+    def __init__(self, cfg, dev, inp, two_phase=False, scales="fp32"):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
+        self.flags = fp8_flag_word(ep, cfg, scales)
+        self.scale_bytes = 1 if scales == "ue8m0" else 4
         N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
         self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
         self.idx_host = torch.from_numpy(inp["topk_idx"])
@@ -272,7 +282,8 @@ class LLWorkload:
         self.ws = torch.empty(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device=dev)
         xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
         self.recv_x = torch.empty((E, R * T, H), dtype=xdt, device=dev)
-        self.recv_s = torch.empty((E, R * T, H // 128), dtype=torch.float32, device=dev) if cfg.fp8 else None
+        self.recv_s = torch.empty((E, R * T, H // 128), dtype=torch.uint8 if scales == "ue8m0" else torch.float32,
+                                  device=dev) if cfg.fp8 else None
         self.recv_src = torch.empty((E, R * T), dtype=torch.int32, device=dev)
         self.recv_count = torch.empty(E, dtype=torch.int32, device=dev)
         self.layout_range = torch.empty((E, R), dtype=torch.int64, device=dev)
@@ -301,7 +312,7 @@ class LLWorkload:
         ep, c = self.ep, self.cfg
         if ev:
             ev[0].record(stream)
-        ep.ep_ll_dispatch_send(x, idx, c.H, c.E, c.R, c.T, c.fp8, self.recv_x, self.recv_s, self.recv_src,
+        ep.ep_ll_dispatch_send(x, idx, c.H, c.E, c.R, c.T, self.flags, self.recv_x, self.recv_s, self.recv_src,
                                self.ws, self.status, stream)
         if ev:
             ev[1].record(stream)
@@ -329,7 +340,7 @@ class LLWorkload:
         c = self.cfg
         N, H, K, R, E = c.N, c.H, c.K, c.R, c.E
         D = self.rows()["received"]
-        row = H + (H // 128) * 4 if c.fp8 else 2 * H
+        row = H + (H // 128) * self.scale_bytes if c.fp8 else 2 * H
         send = N * 2 * H + N * K * 4 + D * row + D * 4 + N * K * 4 + E * R * 8 + E * 4
         recv = 2 * (E * 4 + E * R * 8)
         combine = D * 2 * H + N * K * 8 + N * 2 * H
@@ -354,9 +365,9 @@ def run_ours(args):
         cfg = cfg.scaled(N=args.tokens)
     inp = ei.make_inputs(cfg, seed=0)
     if cfg.mode == "ll":
-        wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase")
+        wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase", scales=args.fp8_scales)
     else:
-        wl = NormalWorkload(cfg, dev, inp)
+        wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lay = wl.layout_for(wl.idx)
@@ -462,7 +473,7 @@ def run_ours(args):
                 "see epinputs for the grouped and Zipf recipes)",
         "config": {"workload": cfg.name, "tokens": N, "hidden": cfg.H, "experts": cfg.E, "topk": cfg.K,
                    "ranks": cfg.R, "max_tokens_per_rank": cfg.T,
-                   "dispatch_dtype": "fp8_e4m3 + fp32 scales / 128 ch" if cfg.fp8 else "bf16",
+                   "dispatch_dtype": (f"fp8_e4m3 + {args.fp8_scales} scales / 128 ch" if cfg.fp8 else "bf16"),
                    "combine_dtype": "bf16 (fp32 accumulation)",
                    "l2": "flushed between steps (256 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

@@ -43,6 +43,10 @@ EP_ST_TIMEOUT = 0x8
 EP_ST_NOT_SENT = 0x10
 EP_ST_MISMATCH = 0x20
 
+EP_FP8 = 0x1
+EP_FP8_ROUND_SCALE = 0x2
+EP_FP8_UE8M0 = 0x4
+
 EP_MAX_EXPERTS = 1024
 EP_MAX_TOPK = 32
 EP_MAX_HIDDEN = 16384
@@ -109,7 +113,7 @@ def lib() -> ctypes.CDLL:
         "ep_combine": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P]),
         "ep_ll_workspace_bytes": (SZ, [I, I, I, I, I]),
         "ep_ll_dispatch_send": (I, [P, P, I, I, I, I, I, I, I, P, P, P, P, SZ, P, P]),
-        "ep_ll_dispatch_recv": (I, [P, SZ, I, I, I, I, I, P, P, P, P]),
+        "ep_ll_dispatch_recv": (I, [P, SZ, I, I, I, I, I, P, P, P, P, P]),
         "ep_ll_combine": (I, [P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_fp8_e4m3_encode": (I, [P, P, I64, P]),
         "ep_ll_combine_send": (I, [P, P, SZ, I, I, I, I, I, I, P, P, P]),
@@ -190,6 +194,13 @@ def new_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int) -> Layo
                   torch.empty((N, num_ranks), **i32), torch.empty((N, K), **i32))
 
 
+def fp8_flags(use_fp8: bool, round_scale: bool = False, use_ue8m0: bool = False) -> int:
+    """The `fp8_flags` argument of ep_dispatch / ep_ll_dispatch_send."""
+    if not use_fp8:
+        return 0
+    return EP_FP8 | (EP_FP8_ROUND_SCALE if round_scale else 0) | (EP_FP8_UE8M0 if use_ue8m0 else 0)
+
+
 def _recv_struct(x, scales=None, src=None, topk_idx=None, topk_w=None) -> ep_recv_buffer_t:
     return ep_recv_buffer_t(_p(x), _p(scales), _p(src), _p(topk_idx), _p(topk_w),
                             x.shape[0] if x is not None else 0)
@@ -211,13 +222,14 @@ def ep_get_dispatch_layout(layout: Layout, workspace: torch.Tensor, status: Opti
                                          _p(status), _stream(stream)), "ep_get_dispatch_layout")
 
 
-def ep_dispatch(layout: Layout, x: torch.Tensor, use_fp8: bool, topk_weights: Optional[torch.Tensor],
+def ep_dispatch(layout: Layout, x: torch.Tensor, fp8: int, topk_weights: Optional[torch.Tensor],
                 rank_buf: Optional[ep_recv_buffer_t], expert_buf: Optional[ep_recv_buffer_t],
                 status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """fp8: 0 / False (BF16), 1 / True (EP_FP8) or an EP_FP8 | ... flags word."""
     c = layout.c_struct()
     rb = ctypes.byref(rank_buf) if rank_buf is not None else None
     eb = ctypes.byref(expert_buf) if expert_buf is not None else None
-    _check(lib().ep_dispatch(ctypes.byref(c), _p(x), x.shape[1], int(use_fp8), _p(topk_weights), rb, eb,
+    _check(lib().ep_dispatch(ctypes.byref(c), _p(x), x.shape[1], int(fp8), _p(topk_weights), rb, eb,
                              _p(status), _stream(stream)), "ep_dispatch")
 
 
@@ -228,18 +240,19 @@ def ep_combine(layout: Layout, expert_y: torch.Tensor, topk_weights: torch.Tenso
                             _p(topk_weights), _p(out), _p(status), _stream(stream)), "ep_combine")
 
 
-def ep_ll_dispatch_send(x, topk_idx, H, E, R, T, use_fp8, recv_x, recv_scales, recv_src, workspace,
+def ep_ll_dispatch_send(x, topk_idx, H, E, R, T, fp8, recv_x, recv_scales, recv_src, workspace,
                         status=None, stream=None) -> None:
     N, K = topk_idx.shape
-    _check(lib().ep_ll_dispatch_send(_p(x), _p(topk_idx), N, K, H, E, R, T, int(use_fp8), _p(recv_x),
+    _check(lib().ep_ll_dispatch_send(_p(x), _p(topk_idx), N, K, H, E, R, T, int(fp8), _p(recv_x),
                                      _p(recv_scales), _p(recv_src), _p(workspace), workspace.numel(),
                                      _p(status), _stream(stream)), "ep_ll_dispatch_send")
 
 
 def ep_ll_dispatch_recv(workspace, N, K, E, R, T, recv_count, layout_range=None, status=None,
-                        stream=None) -> None:
+                        stream=None, cumulative_recv_stats=None) -> None:
     _check(lib().ep_ll_dispatch_recv(_p(workspace), workspace.numel(), N, K, E, R, T, _p(recv_count),
-                                     _p(layout_range), _p(status), _stream(stream)), "ep_ll_dispatch_recv")
+                                     _p(layout_range), _p(cumulative_recv_stats), _p(status), _stream(stream)),
+           "ep_ll_dispatch_recv")
 
 
 def ep_ll_combine(expert_y, topk_weights, workspace, N, K, H, E, R, T, out, status=None,
@@ -298,7 +311,8 @@ class DispatchResult:
 
 def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tensor] = None,
              use_fp8: bool = False, with_rank: bool = True, with_expert: bool = True,
-             exact: bool = False, status: Optional[torch.Tensor] = None, stream=None) -> DispatchResult:
+             exact: bool = False, status: Optional[torch.Tensor] = None, stream=None,
+             round_scale: bool = False, use_ue8m0: bool = False) -> DispatchResult:
     """Scatter x [N, H] bf16 into per-rank and expert-major receive buffers.
 
     exact=False sizes the buffers for the worst case (N*min(K,R) and N*K
@@ -315,12 +329,13 @@ def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tenso
     else:
         cap_r, cap_e = N * min(K, R), N * K
     xdt = torch.uint8 if use_fp8 else torch.bfloat16
+    sdt = torch.uint8 if use_ue8m0 else torch.float32
     S = H // 128
     res = DispatchResult()
     rb = eb = None
     if with_rank:
         res.rank_x = torch.empty((cap_r, H), dtype=xdt, device=dev)
-        res.rank_scales = torch.empty((cap_r, S), dtype=torch.float32, device=dev) if use_fp8 else None
+        res.rank_scales = torch.empty((cap_r, S), dtype=sdt, device=dev) if use_fp8 else None
         res.rank_src = torch.empty(cap_r, dtype=torch.int32, device=dev)
         res.rank_topk_idx = torch.empty((cap_r, K), dtype=torch.int32, device=dev)
         res.rank_topk_weights = torch.empty((cap_r, K), dtype=torch.float32, device=dev) \
@@ -329,11 +344,11 @@ def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tenso
                           res.rank_topk_weights)
     if with_expert:
         res.expert_x = torch.empty((cap_e, H), dtype=xdt, device=dev)
-        res.expert_scales = torch.empty((cap_e, S), dtype=torch.float32, device=dev) if use_fp8 else None
+        res.expert_scales = torch.empty((cap_e, S), dtype=sdt, device=dev) if use_fp8 else None
         res.expert_src = torch.empty(cap_e, dtype=torch.int32, device=dev)
         eb = _recv_struct(res.expert_x, res.expert_scales, res.expert_src)
     tw = topk_weights.contiguous() if topk_weights is not None else None
-    ep_dispatch(layout, x.contiguous(), use_fp8, tw, rb, eb, status, stream)
+    ep_dispatch(layout, x.contiguous(), fp8_flags(use_fp8, round_scale, use_ue8m0), tw, rb, eb, status, stream)
     return res
 
 
@@ -365,7 +380,9 @@ class LLHandle:
 def low_latency_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, num_max_dispatch_tokens_per_rank: int,
                          num_experts: int, num_ranks: int, use_fp8: bool = True,
                          return_recv_hook: bool = True, status: Optional[torch.Tensor] = None,
-                         workspace: Optional[torch.Tensor] = None, stream=None):
+                         workspace: Optional[torch.Tensor] = None, stream=None,
+                         round_scale: bool = False, use_ue8m0: bool = False,
+                         cumulative_local_expert_recv_stats: Optional[torch.Tensor] = None):
     """Fixed-shape low-latency dispatch.
 
     Returns (recv_x, recv_count, handle, hook): recv_x is a [E, R*T, H] bf16
@@ -384,17 +401,19 @@ def low_latency_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, num_max_dispat
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     recv_x = torch.empty((E, R * T, H), dtype=torch.uint8 if use_fp8 else torch.bfloat16, device=dev)
-    recv_scales = torch.empty((E, R * T, H // 128), dtype=torch.float32, device=dev) if use_fp8 else None
+    recv_scales = torch.empty((E, R * T, H // 128), dtype=torch.uint8 if use_ue8m0 else torch.float32,
+                              device=dev) if use_fp8 else None
     recv_src = torch.empty((E, R * T), dtype=torch.int32, device=dev)
     recv_count = torch.empty(E, dtype=torch.int32, device=dev)
     layout_range = torch.empty((E, R), dtype=torch.int64, device=dev)
     idx = topk_idx.to(torch.int32).contiguous()
-    ep_ll_dispatch_send(x.contiguous(), idx, H, E, R, T, use_fp8, recv_x, recv_scales, recv_src, workspace,
-                        status, stream)
+    ep_ll_dispatch_send(x.contiguous(), idx, H, E, R, T, fp8_flags(use_fp8, round_scale, use_ue8m0), recv_x,
+                        recv_scales, recv_src, workspace, status, stream)
     handle = LLHandle(workspace, N, K, H, E, R, T, recv_src, layout_range)
 
     def hook() -> None:
-        ep_ll_dispatch_recv(workspace, N, K, E, R, T, recv_count, layout_range, status, stream)
+        ep_ll_dispatch_recv(workspace, N, K, E, R, T, recv_count, layout_range, status, stream,
+                            cumulative_local_expert_recv_stats)
 
     out_x = (recv_x, recv_scales) if use_fp8 else recv_x
     if not return_recv_hook:

@@ -23,9 +23,16 @@ bool sizes_ok(int N, int K, int E, int R) {
   return true;
 }
 
-bool hidden_ok(int H, int use_fp8) {
+bool hidden_ok(int H, int fp8_flags) {
   if (H < 8 || H > EP_MAX_HIDDEN || H % 8 != 0) return false;
-  if (use_fp8 && H % 128 != 0) return false;
+  if ((fp8_flags & EP_FP8) && H % 128 != 0) return false;
+  return true;
+}
+
+// 0, or EP_FP8 with optional EP_FP8_ROUND_SCALE / EP_FP8_UE8M0.
+bool flags_ok(int f) {
+  if (f & ~(EP_FP8 | EP_FP8_ROUND_SCALE | EP_FP8_UE8M0)) return false;
+  if ((f & (EP_FP8_ROUND_SCALE | EP_FP8_UE8M0)) && !(f & EP_FP8)) return false;
   return true;
 }
 
@@ -143,10 +150,11 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
   return cuda_rc(launch_layout(p, G, true, false, static_cast<cudaStream_t>(stream)));
 }
 
-int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int use_fp8, const float* topk_weights,
+int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, const float* topk_weights,
                 const ep_recv_buffer_t* rank_buf, const ep_recv_buffer_t* expert_buf, int32_t* status,
                 void* stream) {
-  if (!layout_ok(L) || !hidden_ok(hidden, use_fp8)) return EP_ERR_INVALID_ARG;
+  if (!layout_ok(L) || !flags_ok(fp8_flags) || !hidden_ok(hidden, fp8_flags)) return EP_ERR_INVALID_ARG;
+  const int use_fp8 = fp8_flags & EP_FP8;
   const int N = L->num_tokens, K = L->num_topk, E = L->num_experts, R = L->num_ranks;
   if (N > 0 && !x) return EP_ERR_INVALID_ARG;
   if (!aligned16(x)) return EP_ERR_ALIGNMENT;
@@ -157,6 +165,7 @@ int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int use_fp8, co
   p.w = topk_weights;
   p.status = status;
   p.overflow_bit = EP_ST_CAPACITY;
+  p.fp8_flags = fp8_flags;
   if (rank_buf && rank_buf->x) {
     if (N > 0 && !L->rank_slot) return EP_ERR_INVALID_ARG;
     if (rank_buf->capacity < 0) return EP_ERR_INVALID_ARG;
@@ -218,11 +227,12 @@ static int ll_common_checks(int N, int K, int E, int R, int T) {
 }
 
 int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, int H, int E, int R, int T,
-                        int use_fp8, void* recv_x, float* recv_scales, int32_t* recv_src, void* workspace,
+                        int fp8_flags, void* recv_x, void* recv_scales, int32_t* recv_src, void* workspace,
                         size_t workspace_bytes, int32_t* status, void* stream) {
   int rc = ll_common_checks(N, K, E, R, T);
   if (rc != EP_OK) return rc;
-  if (!hidden_ok(H, use_fp8)) return EP_ERR_INVALID_ARG;
+  if (!flags_ok(fp8_flags) || !hidden_ok(H, fp8_flags)) return EP_ERR_INVALID_ARG;
+  const int use_fp8 = fp8_flags & EP_FP8;
   if (!recv_x || (N > 0 && (!x || !topk_idx))) return EP_ERR_INVALID_ARG;
   if (use_fp8 && !recv_scales) return EP_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(recv_x) || (use_fp8 && !aligned16(recv_scales))) return EP_ERR_ALIGNMENT;
@@ -255,6 +265,7 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   dp.expert_slot = at<int32_t>(workspace, w.slot);
   dp.exp_x = static_cast<uint8_t*>(recv_x);
   dp.exp_scales = use_fp8 ? recv_scales : nullptr;
+  dp.fp8_flags = fp8_flags;
   dp.exp_src = recv_src;
   dp.exp_cap = static_cast<int64_t>(E) * R * T;
   dp.exp_src_is_token = 1;
@@ -264,7 +275,8 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
 }
 
 int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int N, int K, int E, int R, int T,
-                        int32_t* recv_count, int64_t* layout_range, int32_t* status, void* stream) {
+                        int32_t* recv_count, int64_t* layout_range, int32_t* cumulative_recv_stats,
+                        int32_t* status, void* stream) {
   int rc = ll_common_checks(N, K, E, R, T);
   if (rc != EP_OK) return rc;
   if (!recv_count) return EP_ERR_INVALID_ARG;
@@ -278,6 +290,7 @@ int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int N, int K, i
   p.expect = LLHeader{kMagicSent, N, K, E, R, T, 0, 0, 0};
   p.recv_count = recv_count;
   p.layout_range = layout_range;
+  p.stats = cumulative_recv_stats;
   p.status = status;
   return cuda_rc(launch_ll_recv(p, E, R, static_cast<cudaStream_t>(stream)));
 }

@@ -165,17 +165,34 @@ constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank c
 
 struct F8Warp {
   uint8_t* xdst[kF8MaxDest];
-  float* sdst[kF8MaxDest];
+  void* sdst[kF8MaxDest];
   float scales[EP_MAX_HIDDEN / 128];
 };
+
+// Smallest power of two >= s for s >= 0 (exact on the bit pattern; a
+// subnormal m * 2^-149 rounds to the next power of two of m).
+__device__ __forceinline__ float pow2_ceil(float s) {
+  unsigned u = __float_as_uint(s);
+  if (u == 0u) return s;
+  if ((u & 0x7F800000u) == 0u) return __uint_as_float(u == 1u ? 1u : (1u << (32 - __clz(u - 1u))));
+  if (u & 0x007FFFFFu) u = (u & 0xFF800000u) + 0x00800000u;
+  return __uint_as_float(u);
+}
+
+// UE8M0 byte 2^(b - 127) of a power-of-two scale >= 2^-127 (0 for s = 0).
+__device__ __forceinline__ uint8_t ue8m0_byte(float s) {
+  return static_cast<uint8_t>((__float_as_uint(s) >> 23) & 0xFFu);
+}
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
 }
 
 // 16 BF16 channels of one lane -> 16 E4M3 codes; the 8 lanes of a 128-channel
-// block share the block's scale s = amax / 448 (all 32 lanes must call it).
-__device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, float& sc) {
+// block share the block's scale s = amax / 448, raised to a power of two with
+// EP_FP8_ROUND_SCALE, and also kept >= 2^-127 with EP_FP8_UE8M0 (all 32 lanes
+// must call it).
+__device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, float& sc, int flags) {
   float f[16];
   f[0] = bf16_lo(v0.x); f[1] = bf16_hi(v0.x); f[2] = bf16_lo(v0.y); f[3] = bf16_hi(v0.y);
   f[4] = bf16_lo(v0.z); f[5] = bf16_hi(v0.z); f[6] = bf16_lo(v0.w); f[7] = bf16_hi(v0.w);
@@ -188,6 +205,8 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   sc = __fdiv_rn(m, 448.0f);
+  if ((flags & (EP_FP8_ROUND_SCALE | EP_FP8_UE8M0)) && sc > 0.0f) sc = pow2_ceil(sc);
+  if ((flags & EP_FP8_UE8M0) && m > 0.0f) sc = fmaxf(sc, __uint_as_float(0x00400000u));  // 2^-127
   if (sc > 0.0f) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
@@ -206,6 +225,8 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
   F8Warp& me = sw[w];
   const int H = p.H, K = p.K, R = p.R, L = p.L, E = p.E;
   const int64_t nsc = H / 128;
+  const bool ue8m0 = p.fp8_flags & EP_FP8_UE8M0;
+  const int64_t ssz = ue8m0 ? 1 : 4;  // bytes per scale
   const int64_t N = p.N;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + w; t < N; t += nw) {
@@ -230,7 +251,8 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
     if (erow >= 0) {
       const int pos = __popc(vm & lanemask_lt());
       me.xdst[pos] = p.exp_x + static_cast<int64_t>(erow) * H;
-      me.sdst[pos] = p.exp_scales ? p.exp_scales + static_cast<int64_t>(erow) * nsc : nullptr;
+      me.sdst[pos] = p.exp_scales ? static_cast<uint8_t*>(p.exp_scales) + static_cast<int64_t>(erow) * nsc * ssz
+                                  : nullptr;
     }
     int n = __popc(vm);
     if (p.rank_x) {
@@ -247,7 +269,9 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
           const int pos = n + __popc(rm & lanemask_lt());
           if (pos < kF8MaxDest) {
             me.xdst[pos] = p.rank_x + static_cast<int64_t>(rrow) * H;
-            me.sdst[pos] = p.rank_scales ? p.rank_scales + static_cast<int64_t>(rrow) * nsc : nullptr;
+            me.sdst[pos] = p.rank_scales
+                               ? static_cast<uint8_t*>(p.rank_scales) + static_cast<int64_t>(rrow) * nsc * ssz
+                               : nullptr;
           }
           if (p.rank_src) p.rank_src[rrow] = static_cast<int32_t>(t);
         }
@@ -279,7 +303,7 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
         v1 = __ldg(reinterpret_cast<const uint4*>(xr + c + 8));
       }
       float sc;
-      const uint4 q = quantize16(v0, v1, sc);
+      const uint4 q = quantize16(v0, v1, sc, p.fp8_flags);
       if (c < H) {
         if ((lane & 7) == 0) me.scales[c >> 7] = sc;
         for (int d = 0; d < n; ++d) st_v4(me.xdst[d] + c, q);
@@ -287,9 +311,12 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
     }
     __syncwarp();
     for (int d = 0; d < n; ++d) {
-      float* sd = me.sdst[d];
-      if (sd)
-        for (int64_t b = lane; b < nsc; b += 32) sd[b] = me.scales[b];
+      void* sd = me.sdst[d];
+      if (!sd) continue;
+      if (ue8m0)
+        for (int64_t b = lane; b < nsc; b += 32) static_cast<uint8_t*>(sd)[b] = ue8m0_byte(me.scales[b]);
+      else
+        for (int64_t b = lane; b < nsc; b += 32) static_cast<float*>(sd)[b] = me.scales[b];
     }
     __syncwarp();
   }

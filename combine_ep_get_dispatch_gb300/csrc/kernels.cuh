@@ -47,16 +47,17 @@ struct DispatchParams {
   const float* w;
   const int32_t* expert_slot;  // [N, K] destination rows (low-latency: slot map)
   const int32_t* rank_slot;    // [N, R] or null
+  int fp8_flags;              // EP_FP8_ROUND_SCALE / EP_FP8_UE8M0 (FP8 kernel only)
   // per-rank buffer (null x: skip)
   uint8_t* rank_x;
-  float* rank_scales;
+  void* rank_scales;          // fp32, or UE8M0 bytes
   int32_t* rank_src;
   int32_t* rank_topk_idx;
   float* rank_topk_w;
   int64_t rank_cap;
   // expert-major buffer (null x: skip)
   uint8_t* exp_x;
-  float* exp_scales;
+  void* exp_scales;
   int32_t* exp_src;
   int64_t exp_cap;
   int exp_src_is_token;  // 1: exp_src[row] = t (low-latency recv_src); 0: t * K + k
@@ -86,6 +87,7 @@ struct LLRecvParams {
   LLHeader expect;
   int32_t* recv_count;
   int64_t* layout_range;
+  int32_t* stats;             // cumulative per-expert receive counts, or null
   int32_t* status;
 };
 

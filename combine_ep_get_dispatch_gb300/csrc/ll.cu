@@ -37,7 +37,11 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParam
   }
   __syncthreads();
   if (!s_ok) return;
-  for (int e = tid; e < E; e += kRecvThreads) p.recv_count[e] = p.count[e];
+  for (int e = tid; e < E; e += kRecvThreads) {
+    const int32_t c = p.count[e];
+    p.recv_count[e] = c;
+    if (p.stats) p.stats[e] += c;  // one block: no other writer
+  }
   if (p.layout_range) {
     const int64_t n = static_cast<int64_t>(E) * R;
     for (int64_t i = tid; i < n; i += kRecvThreads) p.layout_range[i] = p.range[i];

@@ -62,6 +62,18 @@ extern "C" {
 #define EP_ST_NOT_SENT 0x10   /* low-latency receive without a matching send */
 #define EP_ST_MISMATCH 0x20   /* low-latency shapes differ from those of the send */
 
+/* ---- dispatch payload flags (the `fp8_flags` / `use_fp8` arguments) -------
+ * 0: BF16 rows. EP_FP8: E4M3 rows with one fp32 scale per 128 channels,
+ * s = amax / 448. EP_FP8_ROUND_SCALE: s raised to the next power of two, so
+ * dequantisation is an exact shift. EP_FP8_UE8M0: power-of-two scales stored
+ * as one UE8M0 byte 2^(b - 127) per 128 channels ([rows, H/128] bytes; viewed
+ * as int32 [rows, H/512] they are four bytes per word, block b in byte b % 4),
+ * s kept >= 2^-127. ("DeepEP V1 (legacy) guide", section 6.3: round_scale,
+ * use_ue8m0.) The flag values 0 and 1 are the plain BF16 / FP8 choices. */
+#define EP_FP8 0x1
+#define EP_FP8_ROUND_SCALE 0x2
+#define EP_FP8_UE8M0 0x4
+
 /* ---- limits ---------------------------------------------------------- */
 #define EP_MAX_EXPERTS 1024
 #define EP_MAX_TOPK 32
@@ -105,7 +117,8 @@ typedef struct ep_layout {
  * One receive buffer of ep_dispatch. Rows are packed: the per-rank buffer by
  * rank_offset, the expert-major buffer by expert_offset.
  *   x             [capacity, H]       BF16 words, or E4M3 bytes when use_fp8
- *   scales        [capacity, H/128]   fp32 (use_fp8 only; may be NULL to skip)
+ *   scales        [capacity, H/128]   fp32, or UE8M0 bytes with EP_FP8_UE8M0
+ *                                     (FP8 only; may be NULL to skip)
  *   src_idx       [capacity]          int32, may be NULL. Per-rank buffer: the
  *                                     token index t. Expert-major: t * K + k.
  *   topk_idx      [capacity, K]       int32, may be NULL; per-rank buffer only:
@@ -119,7 +132,7 @@ typedef struct ep_layout {
  */
 typedef struct ep_recv_buffer {
   void* x;
-  float* scales;
+  void* scales;
   int32_t* src_idx;
   int32_t* topk_idx;
   float* topk_weights;
@@ -198,13 +211,14 @@ int ep_get_dispatch_layout_noalloc(const ep_layout_t* L, int32_t* status, void* 
  *   L             a handle filled by ep_get_dispatch_layout
  *   x             [N, hidden] BF16
  *   hidden        H: a multiple of 8 (BF16) or of 128 (FP8), <= EP_MAX_HIDDEN
- *   use_fp8       0: rows are copied as BF16; 1: rows are E4M3 + scales
+ *   fp8_flags     0: rows are copied as BF16; EP_FP8 (optionally with
+ *                 EP_FP8_ROUND_SCALE or EP_FP8_UE8M0): rows are E4M3 + scales
  *   topk_weights  [N, K] fp32; needed only for rank_buf->topk_weights
  *   rank_buf      per-rank receive buffer, or NULL to skip the per-rank copy
  *   expert_buf    expert-major receive buffer, or NULL to skip it
  *   status        EP_ST_CAPACITY for rows beyond a buffer's capacity
  */
-int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int use_fp8,
+int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags,
                 const float* topk_weights, const ep_recv_buffer_t* rank_buf,
                 const ep_recv_buffer_t* expert_buf, int32_t* status, void* stream);
 
@@ -253,8 +267,9 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *
  *   x            [N, hidden] BF16
  *   topk_idx     [N, K] int32, -1 = no expert
- *   recv_x       [E, R*T, hidden] BF16, or E4M3 when use_fp8
- *   recv_scales  [E, R*T, hidden/128] fp32 (use_fp8 only)
+ *   fp8_flags    as for ep_dispatch (0 = BF16)
+ *   recv_x       [E, R*T, hidden] BF16, or E4M3 with EP_FP8
+ *   recv_scales  [E, R*T, hidden/128] fp32, or UE8M0 bytes (FP8 only)
  *   recv_src     [E, R*T] int32: global token index of each written row
  *   workspace    at least ep_ll_workspace_bytes(...) bytes; afterwards it
  *                holds the routing that receive and combine use, until the
@@ -265,7 +280,7 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  */
 int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, int num_topk,
                         int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
-                        int use_fp8, void* recv_x, float* recv_scales, int32_t* recv_src,
+                        int fp8_flags, void* recv_x, void* recv_scales, int32_t* recv_src,
                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
@@ -278,6 +293,10 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, 
  *   layout_range  [E, R] int64: (offset << 32) | count of the rows of expert
  *                 e that came from source rank s (offsets are an exclusive
  *                 scan over s); may be NULL
+ *   cumulative_recv_stats  [E] int32 or NULL: each call adds recv_count to it
+ *                 (the per-expert load statistics of "DeepEP V1 (legacy)
+ *                 guide", section 6.3, cumulative_local_expert_recv_stats;
+ *                 rank r's experts are entries [r*E/R, (r+1)*E/R))
  *   status        EP_ST_NOT_SENT if no send filled the workspace since the
  *                 last receive; EP_ST_MISMATCH if the sizes differ from it
  * Must be ordered after the send on the stream (same stream, or an event):
@@ -285,7 +304,8 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, 
  */
 int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int num_tokens, int num_topk,
                         int num_experts, int num_ranks, int max_tokens_per_rank,
-                        int32_t* recv_count, int64_t* layout_range, int32_t* status, void* stream);
+                        int32_t* recv_count, int64_t* layout_range, int32_t* cumulative_recv_stats,
+                        int32_t* status, void* stream);
 
 /*
  * Low-latency combine: out[t] = bf16( sum over k of w[t, k] * y[e][j(t, k)] )

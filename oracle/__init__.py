@@ -44,7 +44,9 @@ def lib():
         L.oracle_bf16_from_f32_n.restype = None
         L.oracle_e4m3_from_f32_n.argtypes = [P, P, i64]
         L.oracle_e4m3_from_f32_n.restype = None
-        L.oracle_quantize_rows.argtypes = [P, i64, i32, P, P]
+        L.oracle_quantize_rows.argtypes = [P, i64, i32, P, P, i32]
+        L.oracle_ue8m0_from_scales.argtypes = [P, i64, P]
+        L.oracle_ue8m0_from_scales.restype = None
         L.oracle_quantize_rows.restype = None
         L.oracle_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
         L.oracle_layout.restype = i32
@@ -66,6 +68,12 @@ def lib():
 
 # Status bits returned by the oracle.
 BAD_INDEX, CAPACITY, LL_OVERFLOW = 1, 2, 4
+# FP8 flags (the library's dispatch flags): E4M3 payload, power-of-two scales, UE8M0 scale bytes.
+FP8, ROUND_SCALE, UE8M0 = 1, 2, 4
+
+
+def fp8_flags(use_fp8: bool, round_scale: bool = False, ue8m0: bool = False) -> int:
+    return (FP8 if use_fp8 else 0) | (ROUND_SCALE if round_scale else 0) | (UE8M0 if ue8m0 else 0)
 
 
 def _p(a: Optional[np.ndarray]):
@@ -99,15 +107,23 @@ def e4m3_to_f64(c: np.ndarray) -> np.ndarray:
     return table[np.asarray(c, dtype=np.uint8)]
 
 
-def quantize_rows(x_bf16: np.ndarray):
+def quantize_rows(x_bf16: np.ndarray, round_scale: bool = False, ue8m0: bool = False):
     """[rows, H] BF16 bits -> (E4M3 codes [rows, H], fp32 scales [rows, H/128])."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     rows, H = x.shape
     assert H % 128 == 0
     q = np.empty((rows, H), dtype=np.uint8)
     s = np.empty((rows, H // 128), dtype=np.float32)
-    lib().oracle_quantize_rows(_p(x), rows, H, _p(q), _p(s))
+    lib().oracle_quantize_rows(_p(x), rows, H, _p(q), _p(s), fp8_flags(True, round_scale, ue8m0))
     return q, s
+
+
+def ue8m0_from_scales(s: np.ndarray) -> np.ndarray:
+    """Power-of-two fp32 scales -> UE8M0 bytes (2^(b - 127)); 0 -> 0."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    out = np.empty(s.shape, np.uint8)
+    lib().oracle_ue8m0_from_scales(_p(s), s.size, _p(out))
+    return out
 
 
 def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
@@ -133,7 +149,8 @@ def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
 
 def dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray, E: int, R: int,
              use_fp8: bool, lay: Optional[dict] = None, rank_cap: Optional[int] = None,
-             exp_cap: Optional[int] = None, with_rank: bool = True, with_expert: bool = True) -> dict:
+             exp_cap: Optional[int] = None, with_rank: bool = True, with_expert: bool = True,
+             round_scale: bool = False, ue8m0: bool = False) -> dict:
     """Per-rank and expert-major receive buffers, sized exactly unless caps are given."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
@@ -147,20 +164,21 @@ def dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray,
     rank_cap = D_r if rank_cap is None else rank_cap
     exp_cap = D_e if exp_cap is None else exp_cap
     xdt = np.uint8 if use_fp8 else np.uint16
+    sdt = np.uint8 if ue8m0 else np.float32
     S = max(H // 128, 1)
     o = {}
     if with_rank:
         o.update(rank_x=np.zeros((rank_cap, H), xdt),
-                 rank_scales=np.zeros((rank_cap, S), np.float32) if use_fp8 else None,
+                 rank_scales=np.zeros((rank_cap, S), sdt) if use_fp8 else None,
                  rank_src=np.full(rank_cap, -1, np.int32),
                  rank_topk_idx=np.full((rank_cap, K), -1, np.int32),
                  rank_topk_weights=np.zeros((rank_cap, K), np.float32))
     if with_expert:
         o.update(exp_x=np.zeros((exp_cap, H), xdt),
-                 exp_scales=np.zeros((exp_cap, S), np.float32) if use_fp8 else None,
+                 exp_scales=np.zeros((exp_cap, S), sdt) if use_fp8 else None,
                  exp_src=np.full(exp_cap, -1, np.int32))
     g = o.get
-    st = lib().oracle_dispatch(_p(x), _p(idx), _p(w), N, K, H, E, R, int(use_fp8),
+    st = lib().oracle_dispatch(_p(x), _p(idx), _p(w), N, K, H, E, R, fp8_flags(use_fp8, round_scale, ue8m0),
                                _p(lay["rank_slot"]), _p(lay["expert_slot"]),
                                _p(g("rank_x")), _p(g("rank_scales")), _p(g("rank_src")),
                                _p(g("rank_topk_idx")), _p(g("rank_topk_weights")), rank_cap,
@@ -183,7 +201,7 @@ def combine(y_bf16: np.ndarray, slot: np.ndarray, topk_weights: np.ndarray) -> t
 
 
 def ll_dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, E: int, R: int, T: int,
-                use_fp8: bool) -> dict:
+                use_fp8: bool, round_scale: bool = False, ue8m0: bool = False) -> dict:
     """Low-latency dispatch into the fixed [E, R*T, H] buffer (global view)."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
@@ -192,13 +210,14 @@ def ll_dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, E: int, R: int, T: int
     xdt = np.uint8 if use_fp8 else np.uint16
     o = {
         "recv_x": np.zeros((E, R * T, H), xdt),
-        "recv_scales": np.zeros((E, R * T, max(H // 128, 1)), np.float32) if use_fp8 else None,
+        "recv_scales": np.zeros((E, R * T, max(H // 128, 1)), np.uint8 if ue8m0 else np.float32)
+        if use_fp8 else None,
         "recv_src": np.full((E, R * T), -1, np.int32),
         "recv_count": np.empty(E, np.int32),
         "layout_range": np.empty((E, R), np.int64),
         "slot_map": np.empty((N, K), np.int32),
     }
-    st = lib().oracle_ll_dispatch(_p(x), _p(idx), N, K, H, E, R, T, int(use_fp8),
+    st = lib().oracle_ll_dispatch(_p(x), _p(idx), N, K, H, E, R, T, fp8_flags(use_fp8, round_scale, ue8m0),
                                   _p(o["recv_x"]), _p(o["recv_scales"]), _p(o["recv_src"]),
                                   _p(o["recv_count"]), _p(o["layout_range"]), _p(o["slot_map"]))
     o["status"] = int(st)

@@ -115,16 +115,39 @@ double e4m3_to_f64(uint8_t c) {
   return s * std::ldexp(1.0 + m / 8.0, field - 7);
 }
 
+// Scale variants ("DeepEP V1 (legacy) guide", section 6.3: round_scale,
+// use_ue8m0). Flag bits as in the library's dispatch flags.
+constexpr int kFp8 = 1, kRoundScale = 2, kUe8m0 = 4;
+
+// Smallest power of two >= s (s > 0), by frexp: s = m * 2^e with m in [0.5, 1).
+float pow2_ceil(float s) {
+  int e;
+  const double m = std::frexp(static_cast<double>(s), &e);
+  return static_cast<float>(m == 0.5 ? static_cast<double>(s) : std::ldexp(1.0, e));
+}
+
+// UE8M0 byte of a power of two s = 2^k: k + 127 (s = 0 -> 0).
+uint8_t ue8m0_of(float s) {
+  if (s == 0.0f) return 0;
+  int e;
+  std::frexp(static_cast<double>(s), &e);  // s = 0.5 * 2^e
+  return static_cast<uint8_t>(e - 1 + 127);
+}
+
 // Per 128-channel block b of one BF16 row: amax_b = max |x|, s_b = amax_b / 448
-// (fp32, round to nearest), q = e4m3(x / s_b).
-void quantize_row(const uint16_t* x, int H, uint8_t* q, float* scales) {
+// (fp32, round to nearest), q = e4m3(x / s_b). With round_scale, s_b is first
+// raised to the next power of two; with UE8M0 it is also kept >= 2^-127 (the
+// smallest UE8M0 value) when the block is not all zero.
+void quantize_row(const uint16_t* x, int H, uint8_t* q, float* scales, int flags = kFp8) {
   for (int b = 0; b < H / 128; ++b) {
     float amax = 0.0f;
     for (int i = 0; i < 128; ++i) {
       const float a = std::fabs(f32_from_bf16(x[b * 128 + i]));
       if (a > amax) amax = a;
     }
-    const float s = amax / 448.0f;
+    float s = amax / 448.0f;
+    if ((flags & (kRoundScale | kUe8m0)) && s > 0.0f) s = pow2_ceil(s);
+    if ((flags & kUe8m0) && amax > 0.0f && s < std::ldexp(1.0f, -127)) s = std::ldexp(1.0f, -127);
     scales[b] = s;
     for (int i = 0; i < 128; ++i) {
       const float xi = f32_from_bf16(x[b * 128 + i]);
@@ -135,14 +158,21 @@ void quantize_row(const uint16_t* x, int H, uint8_t* q, float* scales) {
 
 bool valid_expert(int32_t e, int E) { return e >= 0 && e < E; }
 
-// Copy (or quantise) token t's row into destination row `row` of a receive
-// buffer. `payload` is the token's row already encoded (BF16 or E4M3).
-void write_row(const uint8_t* payload, const float* scales, int H, int use_fp8,
-               void* dst_x, float* dst_scales, int64_t row) {
-  const size_t row_bytes = static_cast<size_t>(H) * (use_fp8 ? 1 : 2);
+// Copy token t's already encoded row (BF16 or E4M3) into destination row
+// `row` of a receive buffer, with its scales: fp32, or UE8M0 bytes.
+void write_row(const uint8_t* payload, const float* scales, int H, int flags,
+               void* dst_x, void* dst_scales, int64_t row) {
+  const bool fp8 = flags & kFp8;
+  const size_t row_bytes = static_cast<size_t>(H) * (fp8 ? 1 : 2);
   std::memcpy(static_cast<uint8_t*>(dst_x) + row * row_bytes, payload, row_bytes);
-  if (use_fp8 && dst_scales)
-    std::memcpy(dst_scales + row * (H / 128), scales, sizeof(float) * (H / 128));
+  if (!fp8 || !dst_scales) return;
+  const int nsc = H / 128;
+  if (flags & kUe8m0) {
+    uint8_t* d = static_cast<uint8_t*>(dst_scales) + row * nsc;
+    for (int b = 0; b < nsc; ++b) d[b] = ue8m0_of(scales[b]);
+  } else {
+    std::memcpy(static_cast<float*>(dst_scales) + row * nsc, scales, sizeof(float) * nsc);
+  }
 }
 
 }  // namespace
@@ -161,10 +191,16 @@ void oracle_e4m3_from_f32_n(const float* in, uint8_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = e4m3_from_f32(in[i]);
 }
 
-// rows x H BF16 -> rows x H E4M3 and rows x H/128 fp32 scales.
-void oracle_quantize_rows(const uint16_t* x, int64_t rows, int H, uint8_t* q, float* scales) {
+// rows x H BF16 -> rows x H E4M3 and rows x H/128 fp32 scales (flags: kFp8
+// plus optional kRoundScale / kUe8m0).
+void oracle_quantize_rows(const uint16_t* x, int64_t rows, int H, uint8_t* q, float* scales, int flags) {
   for (int64_t r = 0; r < rows; ++r)
-    quantize_row(x + r * H, H, q + r * H, scales + r * (H / 128));
+    quantize_row(x + r * H, H, q + r * H, scales + r * (H / 128), flags | kFp8);
+}
+
+// fp32 power-of-two scales -> UE8M0 bytes.
+void oracle_ue8m0_from_scales(const float* s, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = ue8m0_of(s[i]);
 }
 
 // Routing layout.
@@ -229,11 +265,12 @@ int oracle_layout(const int32_t* idx, int N, int K, int E, int R,
 // expert k of t lives on that rank, else -1; topk_w[row,k] = w or 0.
 // Expert-major metadata: src[row] = t*K + k. Any output pointer may be null.
 int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
-                    int N, int K, int H, int E, int R, int use_fp8,
+                    int N, int K, int H, int E, int R, int flags,
                     const int32_t* rank_slot, const int32_t* expert_slot,
-                    void* rank_x, float* rank_scales, int32_t* rank_src,
+                    void* rank_x, void* rank_scales, int32_t* rank_src,
                     int32_t* rank_topk_idx, float* rank_topk_w, int64_t rank_cap,
-                    void* exp_x, float* exp_scales, int32_t* exp_src, int64_t exp_cap) {
+                    void* exp_x, void* exp_scales, int32_t* exp_src, int64_t exp_cap) {
+  const bool use_fp8 = flags & kFp8;
   int status = 0;
   const int L = E / R;
   std::vector<uint8_t> q(H);
@@ -242,14 +279,14 @@ int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
     const uint16_t* xt = x + static_cast<int64_t>(t) * H;
     const uint8_t* payload = reinterpret_cast<const uint8_t*>(xt);
     if (use_fp8) {
-      quantize_row(xt, H, q.data(), sc.data());
+      quantize_row(xt, H, q.data(), sc.data(), flags);
       payload = q.data();
     }
     for (int r = 0; r < R; ++r) {
       const int32_t row = rank_slot[static_cast<int64_t>(t) * R + r];
       if (row < 0) continue;
       if (row >= rank_cap) { status |= kCapacity; continue; }
-      if (rank_x) write_row(payload, sc.data(), H, use_fp8, rank_x, rank_scales, row);
+      if (rank_x) write_row(payload, sc.data(), H, flags, rank_x, rank_scales, row);
       if (rank_src) rank_src[row] = t;
       for (int k = 0; k < K; ++k) {
         const int32_t e = idx[static_cast<int64_t>(t) * K + k];
@@ -262,7 +299,7 @@ int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
       const int32_t row = expert_slot[static_cast<int64_t>(t) * K + k];
       if (row < 0) continue;
       if (row >= exp_cap) { status |= kCapacity; continue; }
-      if (exp_x) write_row(payload, sc.data(), H, use_fp8, exp_x, exp_scales, row);
+      if (exp_x) write_row(payload, sc.data(), H, flags, exp_x, exp_scales, row);
       if (exp_src) exp_src[row] = t * K + k;
     }
   }
@@ -337,8 +374,8 @@ int oracle_combine_staged(const uint16_t* staging, const int32_t* slot, const fl
 //   layout_range[e, s] = (offset << 32) | count for the rows from source s
 //   slot_map[t, k]     = e * R*T + j, or -1 if masked
 int oracle_ll_dispatch(const uint16_t* x, const int32_t* idx, int N, int K, int H,
-                       int E, int R, int T, int use_fp8,
-                       void* recv_x, float* recv_scales, int32_t* recv_src,
+                       int E, int R, int T, int flags,
+                       void* recv_x, void* recv_scales, int32_t* recv_src,
                        int32_t* recv_count, int64_t* layout_range, int32_t* slot_map) {
   int status = 0;
   const int n_s = N / R;
@@ -364,8 +401,8 @@ int oracle_ll_dispatch(const uint16_t* x, const int32_t* idx, int N, int K, int 
       const int64_t row = static_cast<int64_t>(e) * cap + static_cast<int64_t>(j);
       const uint16_t* xt = x + static_cast<int64_t>(t) * H;
       const uint8_t* payload = reinterpret_cast<const uint8_t*>(xt);
-      if (use_fp8) { quantize_row(xt, H, q.data(), sc.data()); payload = q.data(); }
-      write_row(payload, sc.data(), H, use_fp8, recv_x, recv_scales, row);
+      if (flags & kFp8) { quantize_row(xt, H, q.data(), sc.data(), flags); payload = q.data(); }
+      write_row(payload, sc.data(), H, flags, recv_x, recv_scales, row);
       recv_src[row] = t;
       slot_map[static_cast<int64_t>(t) * K + k] = static_cast<int32_t>(row);
       const int s = (n_s > 0) ? t / n_s : 0;

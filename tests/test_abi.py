@@ -85,7 +85,15 @@ def test_host_validation_rejects_before_cuda(L):
         == ep.EP_ERR_WORKSPACE
     assert ll(P(16), P(16), 128, 8, 256, 256, 8, 128, 1, P(16), None, P(16), P(256), 1 << 30, None, None) \
         == ep.EP_ERR_INVALID_ARG  # FP8 without a scale buffer
-    assert L.ep_ll_dispatch_recv(P(256), 16, 128, 8, 256, 8, 128, P(16), None, None, None) == ep.EP_ERR_WORKSPACE
+    assert L.ep_ll_dispatch_recv(P(256), 16, 128, 8, 256, 8, 128, P(16), None, None, None, None) \
+        == ep.EP_ERR_WORKSPACE
+    # FP8 flag words: scale options need EP_FP8; unknown bits are refused
+    assert L.ep_dispatch(ctypes.byref(lay), P(16), 128, ep.EP_FP8_ROUND_SCALE, None, None, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(ctypes.byref(lay), P(16), 128, 0x8 | ep.EP_FP8, None, None, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(ctypes.byref(lay), P(16), 128, ep.EP_FP8 | ep.EP_FP8_UE8M0, None, None, None, None,
+                         None) == ep.EP_OK  # valid flags; no buffer given, so nothing to launch
     assert L.ep_ll_combine(P(16), P(16), P(256), 1 << 30, 128, 8, 100, 256, 8, 128, P(16), None, None) \
         == ep.EP_ERR_INVALID_ARG  # hidden % 8 != 0
     assert L.ep_fp8_e4m3_encode(None, None, -1, None) == ep.EP_ERR_INVALID_ARG

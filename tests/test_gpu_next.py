@@ -137,3 +137,48 @@ def test_normal_path_in_a_cuda_graph():
         assert np.array_equal(u16(out), ref_out)
         assert np.array_equal(lay.expert_slot.cpu().numpy(), ref["layout"]["expert_slot"])
     assert status_value(st) == 0
+
+
+@pytest.mark.parametrize("round_scale,ue8m0", [(True, False), (False, True)])
+def test_dispatch_power_of_two_and_ue8m0_scales(round_scale, ue8m0):
+    cfg = ei.CONFIGS[5].scaled(N=700, H=4096)
+    d = ei.make_inputs(cfg, seed=50)
+    # a few tokens with tiny magnitudes exercise the UE8M0 floor of 2^-127
+    x = d["x"].copy()
+    x[3, :128] = 0x0001
+    x[4, :] = 0
+    st = _status()
+    lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R, status=st)
+    res = ep.dispatch(to_dev_bf16(x), lay, to_dev(d["topk_weights"]), use_fp8=True, exact=True, status=st,
+                      round_scale=round_scale, use_ue8m0=ue8m0)
+    ref = oracle.dispatch(x, d["topk_idx"], d["topk_weights"], cfg.E, cfg.R, True, round_scale=round_scale,
+                          ue8m0=ue8m0)
+    assert np.array_equal(u8(res.expert_x), ref["exp_x"]) and np.array_equal(u8(res.rank_x), ref["rank_x"])
+    got_s = res.expert_scales.cpu().numpy()
+    assert got_s.dtype == (np.uint8 if ue8m0 else np.float32)
+    assert np.array_equal(got_s, ref["exp_scales"]) and np.array_equal(res.rank_scales.cpu().numpy(),
+                                                                         ref["rank_scales"])
+    assert status_value(st) == 0
+
+
+def test_ll_ue8m0_and_cumulative_receive_stats():
+    cfg = ei.CONFIGS[2].scaled(N=32 * 16, H=1024)
+    stats = torch.zeros(cfg.E, dtype=torch.int32, device="cuda")
+    total = np.zeros(cfg.E, np.int64)
+    for seed in (60, 61):
+        d = ei.make_inputs(cfg, seed=seed)
+        st = _status()
+        (rx, rs), cnt, handle, hook = ep.low_latency_dispatch(
+            to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), cfg.T, cfg.E, cfg.R, use_fp8=True, use_ue8m0=True,
+            status=st, cumulative_local_expert_recv_stats=stats)
+        hook()
+        ref = oracle.ll_dispatch(d["x"], d["topk_idx"], cfg.E, cfg.R, cfg.T, True, ue8m0=True)
+        c = cnt.cpu().numpy()
+        assert np.array_equal(c, ref["recv_count"])
+        gx, gs = u8(rx), rs.cpu().numpy()
+        for e in range(cfg.E):
+            assert np.array_equal(gx[e, :c[e]], ref["recv_x"][e, :c[e]])
+            assert np.array_equal(gs[e, :c[e]], ref["recv_scales"][e, :c[e]])
+        total += c
+        assert np.array_equal(stats.cpu().numpy(), total)
+        assert status_value(st) == 0

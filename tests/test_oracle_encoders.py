@@ -147,3 +147,40 @@ def test_quantize_zero_block_keeps_signed_zeros():
     assert q[0, 3] == 0x80 and np.all(np.delete(q[0, :128], 3) == 0)
     assert s[0, 1] == np.float32(1.0) / np.float32(448.0)
     assert q[0, 200] == 0x7E
+
+
+def test_round_scale_is_the_smallest_power_of_two_not_below_amax_over_448():
+    # "DeepEP V1 guide" 6.3: round_scale rounds the scales to powers of two.
+    x = ei.make_x(64, 1024, seed=12)
+    q, s = oracle.quantize_rows(x, round_scale=True)
+    xf = oracle.f32_from_bf16(x).astype(np.float64).reshape(64, 8, 128)
+    amax = np.abs(xf).max(axis=2)
+    s64 = s.astype(np.float64)
+    m, e = np.frexp(s64)
+    assert np.all(m == 0.5)                       # powers of two
+    raw = (amax.astype(np.float32) / np.float32(448.0)).astype(np.float64)
+    assert np.all(s64 >= raw) and np.all(s64 / 2 < raw)
+    # nothing saturates: |x / s| <= 448, and the block max lands in the top binade
+    dq = DEC[q].reshape(64, 8, 128)
+    assert np.all(np.abs(dq).max(axis=2) <= 448.0) and np.all(np.abs(dq).max(axis=2) > 224.0 - 1e-9)
+    v32 = (oracle.f32_from_bf16(x).reshape(64, 8, 128) / s[:, :, None]).astype(np.float32)
+    assert np.array_equal(q.reshape(64, 8, 128), nearest_e4m3(v32))
+
+
+def test_ue8m0_bytes_decode_to_the_scale_and_clamp_tiny_blocks():
+    x = ei.make_x(16, 512, seed=13)
+    q, s = oracle.quantize_rows(x, ue8m0=True)
+    b = oracle.ue8m0_from_scales(s)
+    assert np.array_equal(np.ldexp(1.0, b.astype(np.int64) - 127), s.astype(np.float64))
+    q2, s2 = oracle.quantize_rows(x, round_scale=True)
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)   # normal blocks: same as round_scale
+    # a block whose amax is a BF16 subnormal: the power-of-two scale is below
+    # 2^-127, so UE8M0 clamps it to 2^-127 (byte 0)
+    tiny = np.zeros((1, 128), np.uint16)
+    tiny[0, 5] = 0x0001                      # 2^-133
+    q, s = oracle.quantize_rows(tiny, ue8m0=True)
+    assert s[0, 0] == np.float32(2.0 ** -127) and oracle.ue8m0_from_scales(s)[0, 0] == 0
+    assert q[0, 5] == 0x08 and np.all(np.delete(q[0], 5) == 0)   # 2^-133 / 2^-127 = 2^-6
+    q, s = oracle.quantize_rows(tiny, round_scale=True)
+    assert s[0, 0] < 2.0 ** -127
+    assert oracle.ue8m0_from_scales(np.zeros(3, np.float32)).tolist() == [0, 0, 0]
