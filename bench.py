@@ -58,6 +58,11 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None, help="override the token count (profiling runs)")
     ap.add_argument("--fp8-scales", default="fp32", choices=["fp32", "pow2", "ue8m0"],
                     help="FP8 workloads: fp32 scales, power-of-two fp32 scales, or UE8M0 bytes")
+    ap.add_argument("--expert-alignment", type=int, default=1,
+                    help="normal workloads: pad each expert's segment to a multiple of this many rows")
+    ap.add_argument("--combine-bias", action="store_true", help="add a shared-expert BF16 row in combine")
+    ap.add_argument("--combine", default="flat", choices=["flat", "two-level"],
+                    help="normal workloads: one weighted sum, or per-rank pre-sums then the cross-rank sum")
     ap.add_argument("--ll-combine", default="one-phase", choices=["one-phase", "two-phase"],
                     help="low-latency workloads: combine in one launch, or send + receive hook")
     ap.add_argument("--no-e2e", action="store_true")
@@ -184,11 +189,12 @@ def fp8_flag_word(ep, cfg, scales: str) -> int:
 class NormalWorkload:
     """Layout, dispatch (per-rank + expert-major, BF16 or FP8), combine."""
 
-    def __init__(self, cfg, dev, inp, scales="fp32"):
+    def __init__(self, cfg, dev, inp, scales="fp32", align=1, bias=False, two_level=False):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
         self.flags = fp8_flag_word(ep, cfg, scales)
+        self.align, self.two_level = max(1, align), two_level
         sdt = torch.uint8 if scales == "ue8m0" else torch.float32
         N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
         self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
@@ -197,9 +203,9 @@ class NormalWorkload:
         self.x, self.idx, self.w = self.x_host.to(dev), self.idx_host.to(dev), self.w_host.to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         # Buffers allocated once (worst-case capacities: no host sync in a step).
-        self.lay = ep.new_layout(self.idx, E, R)
+        self.lay = ep.new_layout(self.idx, E, R, self.align)
         self.ws = torch.empty(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device=dev)
-        cap_r, cap_e = N * min(K, R), N * K
+        cap_r, cap_e = N * min(K, R), N * K + E * (self.align - 1)
         xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
         S = H // 128
         self.rank_x = torch.empty((cap_r, H), dtype=xdt, device=dev)
@@ -211,6 +217,8 @@ class NormalWorkload:
         self.exp_s = torch.empty((cap_e, S), dtype=sdt, device=dev) if cfg.fp8 else None
         self.exp_src = torch.empty(cap_e, dtype=torch.int32, device=dev)
         self.out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        self.bias = torch.empty((N, H), dtype=torch.bfloat16, device=dev).normal_() if bias else None
+        self.rank_y = torch.empty((cap_r, H), dtype=torch.bfloat16, device=dev) if two_level else None
         self.rb = ep._recv_struct(self.rank_x, self.rank_s, self.rank_src, self.rank_ti, self.rank_tw)
         self.eb = ep._recv_struct(self.exp_x, self.exp_s, self.exp_src)
         # Expert outputs fed to combine: the BF16 rows themselves (identity
@@ -218,19 +226,21 @@ class NormalWorkload:
         # same expert-major layout (what an expert GEMM would write).
         if cfg.fp8:
             self.y = torch.empty((cap_e, H), dtype=torch.bfloat16, device=dev)
-            lay0 = ep.get_dispatch_layout(self.idx, E, R)
+            lay0 = ep.get_dispatch_layout(self.idx, E, R, expert_alignment=self.align)
             ep.ep_dispatch(lay0, self.x, False, None, None, ep._recv_struct(self.y, None, None))
         else:
             self.y = self.exp_x
-        self.phases = ["layout", "dispatch", "combine"]
+        self.phases = ["layout", "dispatch"] + (["combine_to_ranks", "combine_ranks"] if two_level else ["combine"])
         self.dominant = "dispatch"
         self.kernel_names = {"layout": "layout_kernel", "dispatch": f"dispatch_kernel<{'fp8' if cfg.fp8 else 'bf16'}>",
-                             "combine": "combine_kernel"}
+                             "combine": "combine_kernel", "combine_to_ranks": "combine_to_ranks_kernel",
+                             "combine_ranks": "combine_kernel"}
 
     def layout_for(self, idx):
         L = self.lay
         return self.ep.Layout(idx, L.num_experts, L.num_ranks, L.num_tokens_per_rank, L.num_tokens_per_expert,
-                              L.is_token_in_rank, L.rank_offset, L.expert_offset, L.rank_slot, L.expert_slot)
+                              L.is_token_in_rank, L.rank_offset, L.expert_offset, L.rank_slot, L.expert_slot,
+                              L.expert_alignment)
 
     def run(self, stream, x, idx_layout, w, ev=None):
         ep = self.ep
@@ -242,12 +252,24 @@ class NormalWorkload:
         ep.ep_dispatch(idx_layout, x, self.flags, w, self.rb, self.eb, self.status, stream)
         if ev:
             ev[2].record(stream)
-        ep.ep_combine(idx_layout, self.y, w, self.out, self.status, stream)
+        if self.two_level:
+            ep.ep_combine_to_ranks(idx_layout, self.y, w, self.rank_y, self.status, stream)
+            if ev:
+                ev[3].record(stream)
+            ep.ep_combine_ranks(idx_layout, self.rank_y, self.out, self.status, stream, bias=self.bias)
+            if ev:
+                ev[4].record(stream)
+            return
+        ep.ep_combine(idx_layout, self.y, w, self.out, self.status, stream, bias=self.bias)
         if ev:
             ev[3].record(stream)
 
     def rows(self):
-        return {"per_rank": int(self.lay.rank_offset[-1].item()), "expert_major": int(self.lay.expert_offset[-1].item())}
+        r = {"per_rank": int(self.lay.rank_offset[-1].item()),
+             "expert_major": int(self.lay.num_tokens_per_expert.sum().item())}
+        if self.align > 1:
+            r["padded_expert_major"] = int(self.lay.expert_offset[-1].item())
+        return r
 
     def algorithmic_bytes(self):
         cfg = self.cfg
@@ -260,14 +282,22 @@ class NormalWorkload:
                     + N * K * 4 * 3 + N * R * 4               # idx, w, expert_slot, rank_slot read
                     + (D_r + D_e) * out_row                   # every output row (and its scales) written once
                     + D_e * 4 + D_r * 4 + D_r * K * 8)        # src indices, per-rank top-k idx / weights
-        combine = D_e * 2 * H + N * K * 8 + N * 2 * H         # rows + slots/weights read, out written
+        rows = self.rows()
+        D_pad = rows.get("padded_expert_major", D_e)
+        dispatch += (D_pad - D_e) * out_row                   # zeroed padding rows (aligned layouts)
+        bias_b = N * 2 * H if self.bias is not None else 0
+        if self.two_level:
+            return {"layout": layout, "dispatch": dispatch,
+                    "combine_to_ranks": D_e * 2 * H + N * K * 12 + N * R * 4 + D_r * 2 * H,
+                    "combine_ranks": D_r * 2 * H + N * R * 4 + N * 2 * H + bias_b}
+        combine = D_e * 2 * H + N * K * 8 + N * 2 * H + bias_b  # rows + slots/weights read, out written
         return {"layout": layout, "dispatch": dispatch, "combine": combine}
 
 
 class LLWorkload:
     """Low-latency send, receive (the hook) and combine on the fixed [E, R*T, H] layout."""
 
-    def __init__(self, cfg, dev, inp, two_phase=False, scales="fp32"):
+    def __init__(self, cfg, dev, inp, two_phase=False, scales="fp32", bias=False):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
@@ -288,6 +318,7 @@ class LLWorkload:
         self.recv_count = torch.empty(E, dtype=torch.int32, device=dev)
         self.layout_range = torch.empty((E, R), dtype=torch.int64, device=dev)
         self.out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        self.bias = torch.empty((N, H), dtype=torch.bfloat16, device=dev).normal_() if bias else None
         if cfg.fp8:
             # BF16 expert outputs in the receive layout (what an expert GEMM would write).
             self.y = torch.empty((E, R * T, H), dtype=torch.bfloat16, device=dev)
@@ -325,11 +356,12 @@ class LLWorkload:
             if ev:
                 ev[3].record(stream)
             ep.ep_ll_combine_recv(self.staging, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status,
-                                  stream)
+                                  stream, bias=self.bias)
             if ev:
                 ev[4].record(stream)
             return
-        ep.ep_ll_combine(self.y, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status, stream)
+        ep.ep_ll_combine(self.y, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status, stream,
+                         bias=self.bias)
         if ev:
             ev[3].record(stream)
 
@@ -343,10 +375,11 @@ class LLWorkload:
         row = H + (H // 128) * self.scale_bytes if c.fp8 else 2 * H
         send = N * 2 * H + N * K * 4 + D * row + D * 4 + N * K * 4 + E * R * 8 + E * 4
         recv = 2 * (E * 4 + E * R * 8)
-        combine = D * 2 * H + N * K * 8 + N * 2 * H
+        bias_b = N * 2 * H if self.bias is not None else 0
+        combine = D * 2 * H + N * K * 8 + N * 2 * H + bias_b
         if self.two_phase:
             return {"send": send, "recv": recv, "combine_send": D * 2 * H * 2 + N * K * 4,
-                    "combine_recv": D * 2 * H + N * K * 8 + N * 2 * H}
+                    "combine_recv": D * 2 * H + N * K * 8 + N * 2 * H + bias_b}
         return {"send": send, "recv": recv, "combine": combine}
 
 
@@ -365,9 +398,11 @@ def run_ours(args):
         cfg = cfg.scaled(N=args.tokens)
     inp = ei.make_inputs(cfg, seed=0)
     if cfg.mode == "ll":
-        wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase", scales=args.fp8_scales)
+        wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase", scales=args.fp8_scales,
+                        bias=args.combine_bias)
     else:
-        wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales)
+        wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales, align=args.expert_alignment,
+                            bias=args.combine_bias, two_level=args.combine == "two-level")
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lay = wl.layout_for(wl.idx)
@@ -476,13 +511,17 @@ def run_ours(args):
                    "dispatch_dtype": (f"fp8_e4m3 + {args.fp8_scales} scales / 128 ch" if cfg.fp8 else "bf16"),
                    "combine_dtype": "bf16 (fp32 accumulation)",
                    "l2": "flushed between steps (256 MiB write)",
+                   "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
+                               "combine": args.combine, "ll_combine": args.ll_combine,
+                               "fp8_scales": args.fp8_scales},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "rows": wl.rows()},
         "phases": phases,
         "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind},
-        "gpu_launches": (3 if cfg.mode != "ll" else 3 + len(wl.phases) - 2) * args.steps,
+        "gpu_launches": (len(wl.phases) + (1 if cfg.mode == "ll" else 0)
+                         + (1 if getattr(wl, "align", 1) > 1 else 0)) * args.steps,
         "clocks": sampler.summary(),
     }
     if e2e:

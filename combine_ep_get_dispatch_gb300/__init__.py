@@ -74,6 +74,7 @@ class ep_layout_t(ctypes.Structure):
         ("expert_offset", ctypes.c_void_p),
         ("rank_slot", ctypes.c_void_p),
         ("expert_slot", ctypes.c_void_p),
+        ("expert_alignment", ctypes.c_int32),
     ]
 
 
@@ -110,14 +111,16 @@ def lib() -> ctypes.CDLL:
         "ep_get_dispatch_layout": (I, [ctypes.POINTER(ep_layout_t), P, SZ, P, P]),
         "ep_dispatch": (I, [ctypes.POINTER(ep_layout_t), P, I, I, P, ctypes.POINTER(ep_recv_buffer_t),
                             ctypes.POINTER(ep_recv_buffer_t), P, P]),
-        "ep_combine": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P]),
+        "ep_combine": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P, P]),
+        "ep_combine_to_ranks": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, I64, P, P]),
+        "ep_combine_ranks": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P]),
         "ep_ll_workspace_bytes": (SZ, [I, I, I, I, I]),
         "ep_ll_dispatch_send": (I, [P, P, I, I, I, I, I, I, I, P, P, P, P, SZ, P, P]),
         "ep_ll_dispatch_recv": (I, [P, SZ, I, I, I, I, I, P, P, P, P, P]),
-        "ep_ll_combine": (I, [P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
+        "ep_ll_combine": (I, [P, P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_fp8_e4m3_encode": (I, [P, P, I64, P]),
         "ep_ll_combine_send": (I, [P, P, SZ, I, I, I, I, I, I, P, P, P]),
-        "ep_ll_combine_recv": (I, [P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
+        "ep_ll_combine_recv": (I, [P, P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -169,13 +172,14 @@ class Layout:
     expert_offset: torch.Tensor
     rank_slot: torch.Tensor
     expert_slot: torch.Tensor
+    expert_alignment: int = 1
 
     def c_struct(self) -> ep_layout_t:
         N, K = self.topk_idx.shape
         return ep_layout_t(N, K, self.num_experts, self.num_ranks, _p(self.topk_idx),
                            _p(self.num_tokens_per_rank), _p(self.num_tokens_per_expert),
                            _p(self.is_token_in_rank), _p(self.rank_offset), _p(self.expert_offset),
-                           _p(self.rank_slot), _p(self.expert_slot))
+                           _p(self.rank_slot), _p(self.expert_slot), int(self.expert_alignment))
 
     @property
     def num_recv_tokens_per_expert_list(self) -> torch.Tensor:
@@ -183,7 +187,7 @@ class Layout:
         return self.num_tokens_per_expert.view(self.num_ranks, -1)
 
 
-def new_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int) -> Layout:
+def new_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, expert_alignment: int = 1) -> Layout:
     N, K = topk_idx.shape
     dev = topk_idx.device
     i32 = dict(dtype=torch.int32, device=dev)
@@ -191,7 +195,7 @@ def new_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int) -> Layo
                   torch.empty(num_ranks, **i32), torch.empty(num_experts, **i32),
                   torch.empty((N, num_ranks), dtype=torch.uint8, device=dev),
                   torch.empty(num_ranks + 1, **i32), torch.empty(num_experts + 1, **i32),
-                  torch.empty((N, num_ranks), **i32), torch.empty((N, K), **i32))
+                  torch.empty((N, num_ranks), **i32), torch.empty((N, K), **i32), expert_alignment)
 
 
 def fp8_flags(use_fp8: bool, round_scale: bool = False, use_ue8m0: bool = False) -> int:
@@ -234,10 +238,25 @@ def ep_dispatch(layout: Layout, x: torch.Tensor, fp8: int, topk_weights: Optiona
 
 
 def ep_combine(layout: Layout, expert_y: torch.Tensor, topk_weights: torch.Tensor, out: torch.Tensor,
-               status: Optional[torch.Tensor] = None, stream=None) -> None:
+               status: Optional[torch.Tensor] = None, stream=None, bias: Optional[torch.Tensor] = None) -> None:
     c = layout.c_struct()
     _check(lib().ep_combine(ctypes.byref(c), _p(expert_y), expert_y.shape[0], expert_y.shape[1],
-                            _p(topk_weights), _p(out), _p(status), _stream(stream)), "ep_combine")
+                            _p(topk_weights), _p(bias), _p(out), _p(status), _stream(stream)), "ep_combine")
+
+
+def ep_combine_to_ranks(layout: Layout, expert_y: torch.Tensor, topk_weights: torch.Tensor,
+                        rank_out: torch.Tensor, status: Optional[torch.Tensor] = None, stream=None) -> None:
+    c = layout.c_struct()
+    _check(lib().ep_combine_to_ranks(ctypes.byref(c), _p(expert_y), expert_y.shape[0], expert_y.shape[1],
+                                     _p(topk_weights), _p(rank_out), rank_out.shape[0], _p(status),
+                                     _stream(stream)), "ep_combine_to_ranks")
+
+
+def ep_combine_ranks(layout: Layout, rank_y: torch.Tensor, out: torch.Tensor, status: Optional[torch.Tensor] = None,
+                     stream=None, bias: Optional[torch.Tensor] = None) -> None:
+    c = layout.c_struct()
+    _check(lib().ep_combine_ranks(ctypes.byref(c), _p(rank_y), rank_y.shape[0], rank_y.shape[1], _p(bias),
+                                  _p(out), _p(status), _stream(stream)), "ep_combine_ranks")
 
 
 def ep_ll_dispatch_send(x, topk_idx, H, E, R, T, fp8, recv_x, recv_scales, recv_src, workspace,
@@ -256,9 +275,9 @@ def ep_ll_dispatch_recv(workspace, N, K, E, R, T, recv_count, layout_range=None,
 
 
 def ep_ll_combine(expert_y, topk_weights, workspace, N, K, H, E, R, T, out, status=None,
-                  stream=None) -> None:
-    _check(lib().ep_ll_combine(_p(expert_y), _p(topk_weights), _p(workspace), workspace.numel(), N, K, H,
-                               E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine")
+                  stream=None, bias=None) -> None:
+    _check(lib().ep_ll_combine(_p(expert_y), _p(topk_weights), _p(bias), _p(workspace), workspace.numel(), N, K,
+                               H, E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine")
 
 
 def ep_ll_combine_send(expert_y, workspace, N, K, H, E, R, T, staging, status=None, stream=None) -> None:
@@ -267,9 +286,9 @@ def ep_ll_combine_send(expert_y, workspace, N, K, H, E, R, T, staging, status=No
 
 
 def ep_ll_combine_recv(staging, topk_weights, workspace, N, K, H, E, R, T, out, status=None,
-                       stream=None) -> None:
-    _check(lib().ep_ll_combine_recv(_p(staging), _p(topk_weights), _p(workspace), workspace.numel(), N, K, H,
-                                    E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine_recv")
+                       stream=None, bias=None) -> None:
+    _check(lib().ep_ll_combine_recv(_p(staging), _p(topk_weights), _p(bias), _p(workspace), workspace.numel(), N,
+                                    K, H, E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine_recv")
 
 
 def ep_fp8_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
@@ -283,11 +302,15 @@ def _status(dev) -> torch.Tensor:
 
 def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
                         status: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                        stream=None) -> Layout:
-    """Counts, is_token_in_rank mask and slots for a [N, K] int32 topk_idx."""
+                        stream=None, expert_alignment: int = 1) -> Layout:
+    """Counts, is_token_in_rank mask and slots for a [N, K] int32 topk_idx.
+
+    expert_alignment A > 1 pads each expert's expert-major segment to a
+    multiple of A rows (dispatch zero-fills the padding rows).
+    """
     topk_idx = topk_idx.to(torch.int32).contiguous()
     N, K = topk_idx.shape
-    layout = new_layout(topk_idx, num_experts, num_ranks)
+    layout = new_layout(topk_idx, num_experts, num_ranks, expert_alignment)
     need = ep_layout_workspace_bytes(N, K, num_experts, num_ranks)
     if need == 0:
         raise EPError("get_dispatch_layout", EP_ERR_INVALID_ARG)
@@ -327,7 +350,8 @@ def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tenso
         cap_r = int(layout.rank_offset[-1].item())
         cap_e = int(layout.expert_offset[-1].item())
     else:
-        cap_r, cap_e = N * min(K, R), N * K
+        A = max(1, layout.expert_alignment)
+        cap_r, cap_e = N * min(K, R), N * K + layout.num_experts * (A - 1)
     xdt = torch.uint8 if use_fp8 else torch.bfloat16
     sdt = torch.uint8 if use_ue8m0 else torch.float32
     S = H // 128
@@ -354,13 +378,33 @@ def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tenso
 
 def combine(expert_y: torch.Tensor, layout: Layout, topk_weights: torch.Tensor,
             out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-            stream=None) -> torch.Tensor:
-    """out [N, H] bf16 = sum_k w[t,k] * expert_y[expert_slot[t,k]] (fp32 accumulation)."""
+            stream=None, bias: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """out [N, H] bf16 = sum_k w[t,k] * expert_y[expert_slot[t,k]] (+ bias), fp32 accumulation."""
     N = layout.topk_idx.shape[0]
     if out is None:
         out = torch.empty((N, expert_y.shape[1]), dtype=torch.bfloat16, device=expert_y.device)
-    ep_combine(layout, expert_y.contiguous(), topk_weights.contiguous(), out, status, stream)
+    b = bias.contiguous() if bias is not None else None
+    ep_combine(layout, expert_y.contiguous(), topk_weights.contiguous(), out, status, stream, bias=b)
     return out
+
+
+def combine_two_level(expert_y: torch.Tensor, layout: Layout, topk_weights: torch.Tensor,
+                      bias: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-rank pre-sums (one row per (token, rank)) then the cross-rank sum.
+
+    Returns (out [N, H], rank_rows [D_r, H]); reads the per-rank row count
+    from the layout (one device->host copy).
+    """
+    N = layout.topk_idx.shape[0]
+    H = expert_y.shape[1]
+    D_r = int(layout.rank_offset[-1].item())
+    rank_rows = torch.empty((D_r, H), dtype=torch.bfloat16, device=expert_y.device)
+    ep_combine_to_ranks(layout, expert_y.contiguous(), topk_weights.contiguous(), rank_rows, status, stream)
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=expert_y.device)
+    b = bias.contiguous() if bias is not None else None
+    ep_combine_ranks(layout, rank_rows, out, status, stream, bias=b)
+    return out, rank_rows
 
 
 @dataclasses.dataclass
@@ -424,7 +468,7 @@ def low_latency_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, num_max_dispat
 
 def low_latency_combine(expert_y: torch.Tensor, topk_weights: torch.Tensor, handle: LLHandle,
                         out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                        return_recv_hook: bool = False, stream=None):
+                        return_recv_hook: bool = False, stream=None, bias: Optional[torch.Tensor] = None):
     """out [N, H] bf16 from expert outputs in the [E, R*T, H] receive layout.
 
     return_recv_hook=False: one launch, returns out. True: the send phase
@@ -437,13 +481,14 @@ def low_latency_combine(expert_y: torch.Tensor, topk_weights: torch.Tensor, hand
         out = torch.empty((h.N, h.H), dtype=torch.bfloat16, device=expert_y.device)
     y = expert_y.contiguous()
     w = topk_weights.contiguous()
+    b = bias.contiguous() if bias is not None else None
     if not return_recv_hook:
-        ep_ll_combine(y, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream)
+        ep_ll_combine(y, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream, bias=b)
         return out
     staging = torch.empty((h.N * h.K, h.H), dtype=torch.bfloat16, device=y.device)
     ep_ll_combine_send(y, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, staging, status, stream)
 
     def hook() -> None:
-        ep_ll_combine_recv(staging, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream)
+        ep_ll_combine_recv(staging, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream, bias=b)
 
     return out, hook

@@ -125,6 +125,7 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
   const int N = L->num_tokens, K = L->num_topk, E = L->num_experts, R = L->num_ranks;
   if (!L->num_tokens_per_rank || !L->num_tokens_per_expert || !L->rank_offset || !L->expert_offset)
     return EP_ERR_INVALID_ARG;
+  if (L->expert_alignment < 0 || L->expert_alignment > (1 << 16)) return EP_ERR_INVALID_ARG;
   if (N > 0 && (!L->is_token_in_rank || !L->rank_slot || !L->expert_slot)) return EP_ERR_INVALID_ARG;
   const LayoutWs w = layout_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
@@ -144,6 +145,7 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
   p.expert_off = L->expert_offset;
   p.rank_slot = L->rank_slot;
   p.expert_slot = L->expert_slot;
+  p.align = L->expert_alignment > 1 ? L->expert_alignment : 1;
   p.ws_chunk = at<int32_t>(workspace, w.chunk);
   p.ws_barrier = at<unsigned>(workspace, w.barrier);
   p.status = status;
@@ -192,23 +194,80 @@ int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, 
     p.exp_cap = expert_buf->capacity;
   }
   if (!p.rank_x && !p.exp_x) return EP_OK;
-  return cuda_rc(launch_dispatch(p, use_fp8 != 0, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = cuda_rc(launch_dispatch(p, use_fp8 != 0, s));
+  if (rc != EP_OK || !p.exp_x || L->expert_alignment <= 1) return rc;
+  // Aligned layout: zero the padding rows of the expert-major buffer.
+  PadParams pp{};
+  pp.expert_off = L->expert_offset;
+  pp.per_expert = L->num_tokens_per_expert;
+  pp.E = E;
+  pp.x = p.exp_x;
+  pp.row_bytes = static_cast<int64_t>(hidden) * (use_fp8 ? 1 : 2);
+  pp.scales = static_cast<uint8_t*>(p.exp_scales);
+  pp.scale_row_bytes = static_cast<int64_t>(hidden / 128) * ((fp8_flags & EP_FP8_UE8M0) ? 1 : 4);
+  pp.src = p.exp_src;
+  pp.cap = p.exp_cap;
+  pp.status = status;
+  return cuda_rc(launch_pad_zero(pp, s));
 }
 
 int ep_combine(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,
-               const float* topk_weights, void* out, int32_t* status, void* stream) {
+               const float* topk_weights, const void* bias, void* out, int32_t* status, void* stream) {
   if (!layout_ok(L) || !hidden_ok(hidden, 0) || y_rows < 0) return EP_ERR_INVALID_ARG;
   const int N = L->num_tokens;
   if (N > 0 && (!L->expert_slot || !topk_weights || !out || (!expert_y && y_rows > 0)))
     return EP_ERR_INVALID_ARG;
-  if (!aligned16(expert_y) || !aligned16(out)) return EP_ERR_ALIGNMENT;
+  if (!aligned16(expert_y) || !aligned16(out) || !aligned16(bias)) return EP_ERR_ALIGNMENT;
   CombineParams p{};
   p.y = static_cast<const uint16_t*>(expert_y);
   p.y_rows = y_rows;
   p.slot = L->expert_slot;
   p.w = topk_weights;
+  p.bias = static_cast<const uint16_t*>(bias);
   p.out = static_cast<uint16_t*>(out);
   p.N = N; p.K = L->num_topk; p.H = hidden;
+  p.status = status;
+  return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine_to_ranks(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,
+                        const float* topk_weights, void* rank_out, int64_t rank_rows, int32_t* status,
+                        void* stream) {
+  if (!layout_ok(L) || !hidden_ok(hidden, 0) || y_rows < 0 || rank_rows < 0) return EP_ERR_INVALID_ARG;
+  const int N = L->num_tokens;
+  if (N > 0 && (!L->expert_slot || !L->rank_slot || !topk_weights || !rank_out || (!expert_y && y_rows > 0)))
+    return EP_ERR_INVALID_ARG;
+  if (!aligned16(expert_y) || !aligned16(rank_out)) return EP_ERR_ALIGNMENT;
+  CombineRanksParams p{};
+  p.y = static_cast<const uint16_t*>(expert_y);
+  p.y_rows = y_rows;
+  p.idx = L->topk_idx;
+  p.expert_slot = L->expert_slot;
+  p.rank_slot = L->rank_slot;
+  p.w = topk_weights;
+  p.rank_out = static_cast<uint16_t*>(rank_out);
+  p.rank_rows = rank_rows;
+  p.N = N; p.K = L->num_topk; p.H = hidden; p.E = L->num_experts; p.R = L->num_ranks;
+  p.L = L->num_experts / L->num_ranks;
+  p.status = status;
+  return cuda_rc(launch_combine_to_ranks(p, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine_ranks(const ep_layout_t* L, const void* rank_y, int64_t rank_rows, int hidden, const void* bias,
+                     void* out, int32_t* status, void* stream) {
+  if (!layout_ok(L) || !hidden_ok(hidden, 0) || rank_rows < 0) return EP_ERR_INVALID_ARG;
+  const int N = L->num_tokens;
+  if (N > 0 && (!L->rank_slot || !out || (!rank_y && rank_rows > 0))) return EP_ERR_INVALID_ARG;
+  if (!aligned16(rank_y) || !aligned16(out) || !aligned16(bias)) return EP_ERR_ALIGNMENT;
+  CombineParams p{};
+  p.y = static_cast<const uint16_t*>(rank_y);
+  p.y_rows = rank_rows;
+  p.slot = L->rank_slot;  // [N, R]: the ranks play the role of the slots
+  p.w = nullptr;          // unweighted sum
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.out = static_cast<uint16_t*>(out);
+  p.N = N; p.K = L->num_ranks; p.H = hidden;
   p.status = status;
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
@@ -295,13 +354,14 @@ int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int N, int K, i
   return cuda_rc(launch_ll_recv(p, E, R, static_cast<cudaStream_t>(stream)));
 }
 
-int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* workspace, size_t workspace_bytes,
-                  int N, int K, int H, int E, int R, int T, void* out, int32_t* status, void* stream) {
+int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* bias, const void* workspace,
+                  size_t workspace_bytes, int N, int K, int H, int E, int R, int T, void* out, int32_t* status,
+                  void* stream) {
   int rc = ll_common_checks(N, K, E, R, T);
   if (rc != EP_OK) return rc;
   if (!hidden_ok(H, 0)) return EP_ERR_INVALID_ARG;
   if (!expert_y || (N > 0 && (!topk_weights || !out))) return EP_ERR_INVALID_ARG;
-  if (!aligned16(expert_y) || !aligned16(out)) return EP_ERR_ALIGNMENT;
+  if (!aligned16(expert_y) || !aligned16(out) || !aligned16(bias)) return EP_ERR_ALIGNMENT;
   const LLWs w = ll_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
   void* ws = const_cast<void*>(workspace);
@@ -310,6 +370,7 @@ int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* w
   p.y_rows = static_cast<int64_t>(E) * R * T;
   p.slot = at<int32_t>(ws, w.slot);
   p.w = topk_weights;
+  p.bias = static_cast<const uint16_t*>(bias);
   p.out = static_cast<uint16_t*>(out);
   p.N = N; p.K = K; p.H = H;
   p.ll_hdr = at<LLHeader>(ws, w.hdr);
@@ -341,14 +402,14 @@ int ep_ll_combine_send(const void* expert_y, const void* workspace, size_t works
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
 
-int ep_ll_combine_recv(const void* staging, const float* topk_weights, const void* workspace,
+int ep_ll_combine_recv(const void* staging, const float* topk_weights, const void* bias, const void* workspace,
                        size_t workspace_bytes, int N, int K, int H, int E, int R, int T, void* out,
                        int32_t* status, void* stream) {
   int rc = ll_common_checks(N, K, E, R, T);
   if (rc != EP_OK) return rc;
   if (!hidden_ok(H, 0)) return EP_ERR_INVALID_ARG;
   if (N > 0 && (!staging || !topk_weights || !out)) return EP_ERR_INVALID_ARG;
-  if (!aligned16(staging) || !aligned16(out)) return EP_ERR_ALIGNMENT;
+  if (!aligned16(staging) || !aligned16(out) || !aligned16(bias)) return EP_ERR_ALIGNMENT;
   const LLWs w = ll_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
   void* ws = const_cast<void*>(workspace);
@@ -358,6 +419,7 @@ int ep_ll_combine_recv(const void* staging, const float* topk_weights, const voi
   p.slot = at<int32_t>(ws, w.slot);
   p.token_major = 1;
   p.w = topk_weights;
+  p.bias = static_cast<const uint16_t*>(bias);
   p.out = static_cast<uint16_t*>(out);
   p.N = N; p.K = K; p.H = H;
   p.ll_hdr = at<LLHeader>(ws, w.hdr);

@@ -45,11 +45,12 @@ __device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b)
 // low-latency combine).
 template <bool kGather>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int nchunk) {
-  __shared__ int32_t s_row[EP_MAX_TOPK];
-  __shared__ float s_w[EP_MAX_TOPK];
+  extern __shared__ int32_t s_dyn[];  // K rows, then K weights
   __shared__ int s_ok;
   const int tid = threadIdx.x;
   const int K = p.K, H = p.H;
+  int32_t* s_row = s_dyn;
+  float* s_w = reinterpret_cast<float*>(s_dyn + K);
   if (p.ll_hdr) {
     if (tid == 0) {
       const LLHeader h = *p.ll_hdr;
@@ -72,15 +73,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int64_t t = it / nchunk;
     const int v0 = static_cast<int>(it - t * nchunk) * span;
     const int v1 = min(nvec, v0 + span);
-    if (tid < K) {
-      int32_t row = __ldg(p.slot + t * K + tid);
-      if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + tid);
+    for (int k = tid; k < K; k += kThreads) {
+      int32_t row = __ldg(p.slot + t * K + k);
+      if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + k);
       if (row >= p.y_rows) {
         flag(p.status, EP_ST_CAPACITY);
         row = -1;
       }
-      s_row[tid] = row;
-      s_w[tid] = p.w ? __ldg(p.w + t * K + tid) : 1.0f;
+      s_row[k] = row;
+      s_w[k] = p.w ? __ldg(p.w + t * K + k) : 1.0f;
     }
     __syncthreads();
     for (int v = v0 + tid; v < v1; v += kThreads) {
@@ -148,10 +149,82 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(p.N) * nchunk;
   const int64_t cap = int64_t(1) << 30;
   const int grid = static_cast<int>(items < cap ? items : cap);
+  const size_t smem = static_cast<size_t>(p.K) * 8;
   if (p.gather)
-    combine_kernel<true><<<grid, kThreads, 0, s>>>(p, nchunk);
+    combine_kernel<true><<<grid, kThreads, smem, s>>>(p, nchunk);
   else
-    combine_kernel<false><<<grid, kThreads, 0, s>>>(p, nchunk);
+    combine_kernel<false><<<grid, kThreads, smem, s>>>(p, nchunk);
+  return cudaGetLastError();
+}
+
+// ---- two-level combine, first level --------------------------------------------
+// For every (token, rank) of the mask: rank_out[rank_slot[t, r]] = bf16( sum
+// over k ascending whose expert lives on r of w[t, k] * y[expert_slot[t, k]] )
+// (the reduction DeepEP's expert layer does on each rank before combine).
+// One block per token; the K slots are grouped by rank in shared memory and
+// each rank's chain runs in slot order.
+__global__ void __launch_bounds__(kThreads) combine_to_ranks_kernel(const CombineRanksParams p) {
+  __shared__ int32_t s_row[EP_MAX_TOPK], s_rank[EP_MAX_TOPK], s_out[EP_MAX_TOPK];
+  __shared__ float s_w[EP_MAX_TOPK];
+  const int tid = threadIdx.x;
+  const int K = p.K, H = p.H, E = p.E, L = p.L, R = p.R;
+  const int nvec = H / 8;
+  for (int64_t t = blockIdx.x; t < p.N; t += gridDim.x) {
+    if (tid < K) {
+      const int e = __ldg(p.idx + t * K + tid);
+      int32_t row = __ldg(p.expert_slot + t * K + tid);
+      const bool ok = e >= 0 && e < E && row >= 0;
+      if (ok && row >= p.y_rows) {
+        flag(p.status, EP_ST_CAPACITY);
+        row = -1;
+      }
+      const int r = (ok && row >= 0) ? e / L : -1;
+      s_rank[tid] = r;
+      s_row[tid] = row;
+      s_w[tid] = __ldg(p.w + t * K + tid);
+      int32_t orow = -1;
+      if (r >= 0) {
+        orow = __ldg(p.rank_slot + t * R + r);
+        if (orow >= p.rank_rows) {
+          flag(p.status, EP_ST_CAPACITY);
+          orow = -1;
+        }
+      }
+      s_out[tid] = orow;
+    }
+    __syncthreads();
+    for (int k0 = 0; k0 < K; ++k0) {
+      const int r = s_rank[k0];
+      if (r < 0) continue;
+      bool first = true;
+      for (int k = 0; k < k0; ++k) first &= s_rank[k] != r;
+      if (!first || s_out[k0] < 0) continue;
+      uint16_t* orow = p.rank_out + static_cast<int64_t>(s_out[k0]) * H;
+      for (int v = tid; v < nvec; v += kThreads) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int k = k0; k < K; ++k) {
+          if (s_rank[k] != r) continue;
+          const uint4 yv = __ldg(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(s_row[k]) * H) + v);
+          fma8(acc, s_w[k], yv);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4*>(orow)[v] = o;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s) {
+  if (p.N <= 0) return cudaSuccess;
+  const int64_t cap = int64_t(1) << 30;
+  combine_to_ranks_kernel<<<static_cast<int>(p.N < cap ? p.N : cap), kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@ struct LayoutParams {
   const int32_t* idx;  // [N, K]
   int N, K, E, R, L;
   int tokens_per_cta;
+  int align;                  // expert segments padded to a multiple of `align` rows (1: packed)
   uint32_t magic_L, magic_K;  // ceil(2^32 / d) for d = L, K (0 when d == 1): exact n / d for n < 2^20
   int bits_E, bits_R;         // bits of the largest expert / rank id
   // normal-mode outputs
@@ -80,6 +81,32 @@ struct CombineParams {
   int32_t* status;
 };
 
+struct CombineRanksParams {
+  const uint16_t* y;           // [y_rows, H] expert-major BF16 expert outputs
+  int64_t y_rows;
+  const int32_t* idx;          // [N, K]
+  const int32_t* expert_slot;  // [N, K]
+  const int32_t* rank_slot;    // [N, R]
+  const float* w;              // [N, K]
+  uint16_t* rank_out;          // [rank_rows, H]
+  int64_t rank_rows;
+  int N, K, H, E, R, L;
+  int32_t* status;
+};
+
+struct PadParams {
+  const int32_t* expert_off;   // [E+1] aligned offsets
+  const int32_t* per_expert;   // [E] true counts
+  int E;
+  uint8_t* x;                  // expert-major rows
+  int64_t row_bytes;
+  uint8_t* scales;             // scale rows or null
+  int64_t scale_row_bytes;
+  int32_t* src;                // or null
+  int64_t cap;
+  int32_t* status;
+};
+
 struct LLRecvParams {
   LLHeader* hdr;
   const int32_t* count;   // [E]
@@ -98,6 +125,8 @@ cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll,
 
 cudaError_t launch_dispatch(const DispatchParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s);
+cudaError_t launch_pad_zero(const PadParams& p, cudaStream_t s);
 cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 

@@ -258,6 +258,9 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
         p.per_rank[col - E] = total;
     }
   }
+  // Aligned layouts scan the padded segment lengths (the counts stay true).
+  if (p.align > 1)
+    for (int e = tid; e < E; e += NT) tot[e] = (tot[e] + p.align - 1) / p.align * p.align;
   __syncthreads();
   const int total_e = block_exclusive_scan(tot, E, tmp);
   const int total_r = kRank ? block_exclusive_scan(tot + E, R, tmp) : 0;

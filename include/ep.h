@@ -97,6 +97,14 @@ extern "C" {
  * Slots are deterministic: within a rank (or an expert) rows are in token
  * order (and top-k order for repeated experts), ranks (experts) in index
  * order.
+ *
+ * expert_alignment A > 1 pads every expert's segment of the expert-major
+ * buffer to a multiple of A rows ("DeepEP Ascend deep dive", "Dispatch's
+ * Three Phases": expert alignment to 128 rows for the grouped GEMM, empty rows
+ * filled with zeros): expert_offset becomes the exclusive scan of the padded
+ * lengths (num_tokens_per_expert stays the true count) and ep_dispatch zeroes
+ * the padding rows (payload, scales, src = -1). Capacity then needs
+ * N * K + E * (A - 1) rows in the worst case.
  */
 typedef struct ep_layout {
   int32_t num_tokens;  /* N >= 0 */
@@ -111,6 +119,8 @@ typedef struct ep_layout {
   int32_t* expert_offset;
   int32_t* rank_slot;
   int32_t* expert_slot;
+  int32_t expert_alignment; /* 0 or 1: expert segments packed; A > 1: each
+                               expert's segment padded to a multiple of A rows */
 } ep_layout_t;
 
 /*
@@ -239,10 +249,46 @@ int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags,
  *                 flagged EP_ST_CAPACITY
  *   hidden        a multiple of 8, <= EP_MAX_HIDDEN
  *   topk_weights  [N, K] fp32 router weights
+ *   bias          [N, hidden] BF16 or NULL: added in fp32 after the weighted
+ *                 sum, before the BF16 rounding (the shared expert's output
+ *                 folded into the epilogue, "DeepEP Ascend deep dive",
+ *                 "Combine: More Output, Same Cost")
  *   out           [N, hidden] BF16
  */
 int ep_combine(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,
-               const float* topk_weights, void* out, int32_t* status, void* stream);
+               const float* topk_weights, const void* bias, void* out, int32_t* status,
+               void* stream);
+
+/*
+ * Two-level combine, first level: each rank reduces its own experts' outputs
+ * before sending one row per (token, rank) back (the shape of DeepEP's normal
+ * combine(x, handle), whose x is one row per received token of each rank,
+ * "DeepEP V1 (legacy) guide", section 5.1). For every (t, r) with
+ * is_token_in_rank[t, r]: rank_out[rank_slot[t, r]] = bf16( sum over k in slot
+ * order whose expert lives on r of w[t, k] * y[expert_slot[t, k]] ), the fp32
+ * fused multiply-add chain of ep_combine.
+ *
+ *   L             a handle filled by ep_get_dispatch_layout (K <= EP_MAX_TOPK)
+ *   expert_y      [y_rows, hidden] BF16 expert outputs, expert-major
+ *   topk_weights  [N, K] fp32
+ *   rank_out      [rank_rows, hidden] BF16, the per-rank layout
+ */
+int ep_combine_to_ranks(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,
+                        const float* topk_weights, void* rank_out, int64_t rank_rows,
+                        int32_t* status, void* stream);
+
+/*
+ * Two-level combine, second level: out[t] = bf16( sum over ranks r ascending
+ * with is_token_in_rank[t, r] of rank_y[rank_slot[t, r]] (+ bias) ), fp32
+ * accumulation, one rounding. With rank_y from ep_combine_to_ranks this is the
+ * whole combine with one intermediate BF16 rounding per rank.
+ *
+ *   rank_y   [rank_rows, hidden] BF16 per-rank rows
+ *   bias     [N, hidden] BF16 or NULL, as for ep_combine
+ *   out      [N, hidden] BF16
+ */
+int ep_combine_ranks(const ep_layout_t* L, const void* rank_y, int64_t rank_rows, int hidden,
+                     const void* bias, void* out, int32_t* status, void* stream);
 
 /*
  * Bytes of device workspace the low-latency calls need. The workspace
@@ -316,13 +362,14 @@ int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int num_tokens,
  *
  *   expert_y      [E, R*T, hidden] BF16 expert outputs in the receive layout
  *   topk_weights  [N, K] fp32
+ *   bias          [N, hidden] BF16 or NULL, as for ep_combine
  *   workspace     filled by the send of this batch (same sizes)
  *   out           [N, hidden] BF16
  *   status        EP_ST_NOT_SENT / EP_ST_MISMATCH as for the receive
  */
-int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* workspace,
-                  size_t workspace_bytes, int num_tokens, int num_topk, int hidden,
-                  int num_experts, int num_ranks, int max_tokens_per_rank, void* out,
+int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* bias,
+                  const void* workspace, size_t workspace_bytes, int num_tokens, int num_topk,
+                  int hidden, int num_experts, int num_ranks, int max_tokens_per_rank, void* out,
                   int32_t* status, void* stream);
 
 /*
@@ -352,14 +399,15 @@ int ep_ll_combine_send(const void* expert_y, const void* workspace, size_t works
  *
  *   staging       [N * K, hidden] BF16 written by ep_ll_combine_send
  *   topk_weights  [N, K] fp32
+ *   bias          [N, hidden] BF16 or NULL, as for ep_combine
  *   workspace     the same workspace (it says which slots are masked)
  *   out           [N, hidden] BF16
  * Must be ordered after the send phase on the stream.
  */
-int ep_ll_combine_recv(const void* staging, const float* topk_weights, const void* workspace,
-                       size_t workspace_bytes, int num_tokens, int num_topk, int hidden,
-                       int num_experts, int num_ranks, int max_tokens_per_rank, void* out,
-                       int32_t* status, void* stream);
+int ep_ll_combine_recv(const void* staging, const float* topk_weights, const void* bias,
+                       const void* workspace, size_t workspace_bytes, int num_tokens, int num_topk,
+                       int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
+                       void* out, int32_t* status, void* stream);
 
 /*
  * Element-wise fp32 -> FP8 E4M3 conversion (round to nearest even, saturated

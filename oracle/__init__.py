@@ -48,12 +48,14 @@ def lib():
         L.oracle_ue8m0_from_scales.argtypes = [P, i64, P]
         L.oracle_ue8m0_from_scales.restype = None
         L.oracle_quantize_rows.restype = None
-        L.oracle_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
+        L.oracle_layout.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
         L.oracle_layout.restype = i32
         L.oracle_dispatch.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P,
                                       P, P, P, P, P, i64, P, P, P, i64]
         L.oracle_dispatch.restype = i32
-        L.oracle_combine.argtypes = [P, i64, P, P, i32, i32, i32, P]
+        L.oracle_combine.argtypes = [P, i64, P, P, P, i32, i32, i32, P]
+        L.oracle_combine_to_ranks.argtypes = [P, i64, P, P, P, P, i32, i32, i32, i32, i32, P, i64]
+        L.oracle_combine_to_ranks.restype = i32
         L.oracle_combine.restype = i32
         L.oracle_ll_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32,
                                          P, P, P, P, P, P]
@@ -126,7 +128,7 @@ def ue8m0_from_scales(s: np.ndarray) -> np.ndarray:
     return out
 
 
-def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
+def layout(topk_idx: np.ndarray, E: int, R: int, expert_alignment: int = 1) -> dict:
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
     N, K = idx.shape
     assert E % R == 0
@@ -139,7 +141,7 @@ def layout(topk_idx: np.ndarray, E: int, R: int) -> dict:
         "rank_slot": np.empty((N, R), np.int32),
         "expert_slot": np.empty((N, K), np.int32),
     }
-    st = lib().oracle_layout(_p(idx), N, K, E, R, _p(o["num_tokens_per_rank"]),
+    st = lib().oracle_layout(_p(idx), N, K, E, R, expert_alignment, _p(o["num_tokens_per_rank"]),
                              _p(o["num_tokens_per_expert"]), _p(o["is_token_in_rank"]),
                              _p(o["rank_offset"]), _p(o["expert_offset"]),
                              _p(o["rank_slot"]), _p(o["expert_slot"]))
@@ -188,15 +190,35 @@ def dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray,
     return o
 
 
-def combine(y_bf16: np.ndarray, slot: np.ndarray, topk_weights: np.ndarray) -> tuple:
-    """out [N, H] BF16 bits from expert outputs y [rows, H] and slot map [N, K]."""
+def combine(y_bf16: np.ndarray, slot: np.ndarray, topk_weights: Optional[np.ndarray],
+            bias: Optional[np.ndarray] = None) -> tuple:
+    """out [N, H] BF16 bits from expert outputs y [rows, H] and slot map [N, K].
+
+    topk_weights None: every weight is 1. bias [N, H] BF16 is added after the sum.
+    """
     y = np.ascontiguousarray(y_bf16, dtype=np.uint16).reshape(-1, y_bf16.shape[-1])
     slot = np.ascontiguousarray(slot, dtype=np.int32)
-    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.uint16)
     N, K = slot.shape
     H = y.shape[1]
     out = np.empty((N, H), np.uint16)
-    st = lib().oracle_combine(_p(y), y.shape[0], _p(slot), _p(w), N, K, H, _p(out))
+    st = lib().oracle_combine(_p(y), y.shape[0], _p(slot), _p(w), _p(b), N, K, H, _p(out))
+    return out, int(st)
+
+
+def combine_to_ranks(y_bf16: np.ndarray, topk_idx: np.ndarray, lay: dict, topk_weights: np.ndarray,
+                     E: int, R: int) -> tuple:
+    """Per-rank weighted pre-sums [D_r, H]: row rank_slot[t, r] sums t's experts on rank r."""
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    N, K = idx.shape
+    H = y.shape[1]
+    D_r = int(lay["rank_offset"][-1])
+    out = np.zeros((D_r, H), np.uint16)
+    st = lib().oracle_combine_to_ranks(_p(y), y.shape[0], _p(idx), _p(lay["expert_slot"]), _p(lay["rank_slot"]),
+                                       _p(w), N, K, E, R, H, _p(out), D_r)
     return out, int(st)
 
 

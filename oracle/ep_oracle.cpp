@@ -211,7 +211,7 @@ void oracle_ue8m0_from_scales(const float* s, int64_t n, uint8_t* out) {
 //   expert_slot[t,k] = expert_off[e] + position of (t,k) in expert e's list
 //   rank_slot[t,r]   = rank_off[r] + position of t in rank r's list
 // Lists are built by visiting (t, k) in order, so they are in token order.
-int oracle_layout(const int32_t* idx, int N, int K, int E, int R,
+int oracle_layout(const int32_t* idx, int N, int K, int E, int R, int expert_alignment,
                   int32_t* per_rank, int32_t* per_expert, uint8_t* mask,
                   int32_t* rank_off, int32_t* expert_off,
                   int32_t* rank_slot, int32_t* expert_slot) {
@@ -231,10 +231,15 @@ int oracle_layout(const int32_t* idx, int N, int K, int E, int R,
       if (!seen[r]) { seen[r] = 1; rank_list[r].push_back(t); }
     }
   }
+  // With an alignment A > 1 each expert's segment is padded to a multiple of
+  // A rows ("DeepEP Ascend deep dive", "Dispatch's Three Phases": expert
+  // alignment to 128 for the grouped GEMM; the padding rows are zeros).
+  const int A = expert_alignment > 1 ? expert_alignment : 1;
   expert_off[0] = 0;
   for (int e = 0; e < E; ++e) {
     per_expert[e] = static_cast<int32_t>(expert_list[e].size());
-    expert_off[e + 1] = expert_off[e] + per_expert[e];
+    const int32_t seg = (per_expert[e] + A - 1) / A * A;
+    expert_off[e + 1] = expert_off[e] + seg;
   }
   rank_off[0] = 0;
   for (int r = 0; r < R; ++r) {
@@ -308,9 +313,12 @@ int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
 
 // Combine: out[t] = bf16( sum over k ascending with slot[t,k] >= 0 of
 // w[t,k] * y[slot[t,k]] ), each term added with one fp32 fused multiply-add
-// onto an accumulator that starts at +0.
+// onto an accumulator that starts at +0. An optional bias row (the shared
+// expert's output, "DeepEP Ascend deep dive", "Combine: More Output, Same
+// Cost") is added in fp32 after the last term, before the one BF16 rounding.
+// w may be null: every weight is 1.
 int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const float* w,
-                   int N, int K, int H, uint16_t* out) {
+                   const uint16_t* bias, int N, int K, int H, uint16_t* out) {
   int status = 0;
   std::vector<float> acc(H);
   for (int t = 0; t < N; ++t) {
@@ -319,12 +327,45 @@ int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const
       const int32_t row = slot[static_cast<int64_t>(t) * K + k];
       if (row < 0) continue;
       if (row >= y_rows) { status |= kCapacity; continue; }
-      const float wk = w[static_cast<int64_t>(t) * K + k];
+      const float wk = w ? w[static_cast<int64_t>(t) * K + k] : 1.0f;
       const uint16_t* yr = y + static_cast<int64_t>(row) * H;
       for (int h = 0; h < H; ++h) acc[h] = std::fmaf(wk, f32_from_bf16(yr[h]), acc[h]);
     }
+    if (bias)
+      for (int h = 0; h < H; ++h) acc[h] = acc[h] + f32_from_bf16(bias[static_cast<int64_t>(t) * H + h]);
     for (int h = 0; h < H; ++h) out[static_cast<int64_t>(t) * H + h] = bf16_from_f32(acc[h]);
   }
+  return status;
+}
+
+// Two-level combine, first level (the expert layer's reduction on each rank,
+// as in DeepEP's normal combine(x, handle), "DeepEP V1 (legacy) guide" 5.1):
+// for every (t, r) in the mask, rank_out[rank_slot[t,r]] = bf16( sum over k
+// ascending whose expert lives on r of w[t,k] * y[expert_slot[t,k]] ).
+int oracle_combine_to_ranks(const uint16_t* y, int64_t y_rows, const int32_t* idx, const int32_t* expert_slot,
+                            const int32_t* rank_slot, const float* w, int N, int K, int E, int R, int H,
+                            uint16_t* rank_out, int64_t rank_rows) {
+  int status = 0;
+  const int L = E / R;
+  std::vector<float> acc(H);
+  for (int t = 0; t < N; ++t)
+    for (int r = 0; r < R; ++r) {
+      const int32_t orow = rank_slot[static_cast<int64_t>(t) * R + r];
+      if (orow < 0) continue;
+      if (orow >= rank_rows) { status |= kCapacity; continue; }
+      std::fill(acc.begin(), acc.end(), 0.0f);
+      for (int k = 0; k < K; ++k) {
+        const int64_t tk = static_cast<int64_t>(t) * K + k;
+        const int32_t e = idx[tk];
+        if (!valid_expert(e, E) || e / L != r) continue;
+        const int32_t row = expert_slot[tk];
+        if (row < 0) continue;
+        if (row >= y_rows) { status |= kCapacity; continue; }
+        for (int h = 0; h < H; ++h)
+          acc[h] = std::fmaf(w[tk], f32_from_bf16(y[static_cast<int64_t>(row) * H + h]), acc[h]);
+      }
+      for (int h = 0; h < H; ++h) rank_out[static_cast<int64_t>(orow) * H + h] = bf16_from_f32(acc[h]);
+    }
   return status;
 }
 

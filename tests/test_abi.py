@@ -74,7 +74,11 @@ def test_host_validation_rejects_before_cuda(L):
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 64, 1, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 32768, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
     # combine: misaligned output
-    assert L.ep_combine(ctypes.byref(lay), P(16), 10, 64, P(16), P(24), None, None) == ep.EP_ERR_ALIGNMENT
+    assert L.ep_combine(ctypes.byref(lay), P(16), 10, 64, P(16), None, P(24), None, None) == ep.EP_ERR_ALIGNMENT
+    assert L.ep_combine(ctypes.byref(lay), P(16), 10, 64, P(16), P(40), P(32), None, None) == ep.EP_ERR_ALIGNMENT
+    # alignment of the expert segments must be sane
+    bad = ep.ep_layout_t(10, 8, 256, 8, P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16), -3)
+    assert L.ep_get_dispatch_layout(ctypes.byref(bad), P(256), 1 << 20, None, None) == ep.EP_ERR_INVALID_ARG
     # low latency: tokens per rank above T, N not divisible by R, missing workspace
     ll = L.ep_ll_dispatch_send
     assert ll(P(16), P(16), 160, 8, 256, 256, 8, 16, 0, P(16), None, P(16), P(256), 1 << 30, None, None) \
@@ -94,7 +98,7 @@ def test_host_validation_rejects_before_cuda(L):
         == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 128, ep.EP_FP8 | ep.EP_FP8_UE8M0, None, None, None, None,
                          None) == ep.EP_OK  # valid flags; no buffer given, so nothing to launch
-    assert L.ep_ll_combine(P(16), P(16), P(256), 1 << 30, 128, 8, 100, 256, 8, 128, P(16), None, None) \
+    assert L.ep_ll_combine(P(16), P(16), None, P(256), 1 << 30, 128, 8, 100, 256, 8, 128, P(16), None, None) \
         == ep.EP_ERR_INVALID_ARG  # hidden % 8 != 0
     assert L.ep_fp8_e4m3_encode(None, None, -1, None) == ep.EP_ERR_INVALID_ARG
 

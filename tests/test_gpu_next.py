@@ -182,3 +182,77 @@ def test_ll_ue8m0_and_cumulative_receive_stats():
         total += c
         assert np.array_equal(stats.cpu().numpy(), total)
         assert status_value(st) == 0
+
+
+def test_combine_with_shared_expert_bias():
+    cfg = ei.CONFIGS[3].scaled(N=600, H=2048)
+    idx, w = ei.make_routing(cfg, seed=70)
+    lay_ref = oracle.layout(idx, cfg.E, cfg.R)
+    D_e = int(lay_ref["expert_offset"][-1])
+    y = _expert_outputs((D_e, cfg.H), seed=70)
+    bias = _expert_outputs((cfg.N, cfg.H), seed=71)
+    st = _status()
+    lay = ep.get_dispatch_layout(to_dev(idx), cfg.E, cfg.R, status=st)
+    out = ep.combine(to_dev_bf16(y), lay, to_dev(w), status=st, bias=to_dev_bf16(bias))
+    ref, _ = oracle.combine(y, lay_ref["expert_slot"], w, bias)
+    assert np.array_equal(u16(out), ref)
+    # low latency, one launch and two phases
+    lcfg = ei.CONFIGS[1].scaled(H=1024)
+    d = ei.make_inputs(lcfg, seed=72)
+    recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), lcfg.T, lcfg.E,
+                                                      lcfg.R, use_fp8=False, status=st)
+    hook()
+    lref = oracle.ll_dispatch(d["x"], d["topk_idx"], lcfg.E, lcfg.R, lcfg.T, False)
+    b2 = _expert_outputs((lcfg.N, lcfg.H), seed=73)
+    one = ep.low_latency_combine(recv, to_dev(d["topk_weights"]), handle, status=st, bias=to_dev_bf16(b2))
+    two, h2 = ep.low_latency_combine(recv, to_dev(d["topk_weights"]), handle, status=st, bias=to_dev_bf16(b2),
+                                     return_recv_hook=True)
+    h2()
+    want, _ = oracle.combine(lref["recv_x"].reshape(-1, lcfg.H), lref["slot_map"], d["topk_weights"], b2)
+    assert np.array_equal(u16(one), want) and np.array_equal(u16(two), want)
+    assert status_value(st) == 0
+
+
+@pytest.mark.parametrize("A,fp8,ue8m0", [(128, False, False), (128, True, False), (2, True, True)])
+def test_aligned_expert_layout_and_zero_padding(A, fp8, ue8m0):
+    cfg = ei.CONFIGS[5].scaled(N=900, H=1024)
+    d = ei.make_inputs(cfg, seed=80)
+    st = _status()
+    lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R, status=st, expert_alignment=A)
+    ref_lay = oracle.layout(d["topk_idx"], cfg.E, cfg.R, expert_alignment=A)
+    for k in ("num_tokens_per_expert", "expert_offset", "expert_slot", "rank_slot", "rank_offset"):
+        assert np.array_equal(getattr(lay, k).cpu().numpy(), ref_lay[k]), k
+    D_e = int(ref_lay["expert_offset"][-1])
+    # poison the buffers so the zero padding is visible
+    res = ep.dispatch(to_dev_bf16(d["x"]), lay, to_dev(d["topk_weights"]), use_fp8=fp8, with_rank=False,
+                      status=st, use_ue8m0=ue8m0)
+    ref = oracle.dispatch(d["x"], d["topk_idx"], d["topk_weights"], cfg.E, cfg.R, fp8, lay=ref_lay,
+                          with_rank=False, ue8m0=ue8m0)
+    conv = u8 if fp8 else u16
+    assert np.array_equal(conv(res.expert_x[:D_e]), ref["exp_x"])
+    assert np.array_equal(res.expert_src[:D_e].cpu().numpy(), ref["exp_src"])
+    if fp8:
+        assert np.array_equal(res.expert_scales[:D_e].cpu().numpy(), ref["exp_scales"])
+    # combine still reads the real rows
+    y = _expert_outputs((D_e, cfg.H), seed=81)
+    out = ep.combine(to_dev_bf16(y), lay, to_dev(d["topk_weights"]), status=st)
+    want, _ = oracle.combine(y, ref_lay["expert_slot"], d["topk_weights"])
+    assert np.array_equal(u16(out), want)
+    assert status_value(st) == 0
+
+
+def test_two_level_combine_matches_oracle():
+    cfg = ei.CONFIGS[3].scaled(N=800, H=1024)
+    idx, w = ei.make_routing(cfg, seed=90)
+    lay_ref = oracle.layout(idx, cfg.E, cfg.R)
+    D_e = int(lay_ref["expert_offset"][-1])
+    y = _expert_outputs((D_e, cfg.H), seed=90)
+    bias = _expert_outputs((cfg.N, cfg.H), seed=91)
+    st = _status()
+    lay = ep.get_dispatch_layout(to_dev(idx), cfg.E, cfg.R, status=st)
+    out, rank_rows = ep.combine_two_level(to_dev_bf16(y), lay, to_dev(w), bias=to_dev_bf16(bias), status=st)
+    part, _ = oracle.combine_to_ranks(y, idx, lay_ref, w, cfg.E, cfg.R)
+    assert np.array_equal(u16(rank_rows), part)
+    want, _ = oracle.combine(part, lay_ref["rank_slot"], None, bias)
+    assert np.array_equal(u16(out), want)
+    assert status_value(st) == 0

@@ -258,3 +258,96 @@ def test_two_phase_ll_combine_equals_single_phase():
     two = oracle.ll_combine_recv(staging, ll["slot_map"], w)
     one, _ = oracle.ll_combine(y, ll["slot_map"], w)
     assert np.array_equal(two, one)
+
+
+def test_bias_is_added_after_the_weighted_sum():
+    # "DeepEP Ascend deep dive", "Combine: More Output, Same Cost": the shared
+    # expert's output is added as a bias in the epilogue. Hand-derived: terms
+    # 2^24 and 1 first give 2^24 in fp32 (2^24 + 1 rounds to even), then the
+    # bias -2^24 leaves 0; adding the bias first would leave 1.
+    y = ei.bf16_bits_from_f32(np.array([[1.0], [1.0]], np.float32))
+    slot = np.array([[0, 1]], np.int32)
+    w = np.array([[2.0 ** 24, 1.0]], np.float32)
+    bias = ei.bf16_bits_from_f32(np.array([[-(2.0 ** 24)]], np.float32))
+    out, _ = oracle.combine(y, slot, w, bias)
+    assert oracle.f32_from_bf16(out)[0, 0] == 0.0
+    # zero bias changes nothing; masked tokens give the bias itself
+    cfg = _small(4, 200, 256)
+    x, idx, w = _inputs(cfg)
+    lay = oracle.layout(idx, cfg.E, cfg.R)
+    y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(3, 5), int(lay["expert_offset"][-1]) * 256)
+                              .astype(np.float32)).reshape(-1, 256)
+    a, _ = oracle.combine(y, lay["expert_slot"], w)
+    b, _ = oracle.combine(y, lay["expert_slot"], w, np.zeros_like(x))
+    assert np.array_equal(a, b)
+    none = np.full_like(lay["expert_slot"], -1)
+    c, _ = oracle.combine(y, none, w, x)
+    assert np.array_equal(c, x)
+
+
+@pytest.mark.parametrize("A", [2, 128])
+def test_expert_alignment_pads_each_segment(A):
+    cfg = _small(5, 600, 256)
+    x, idx, w = _inputs(cfg)
+    plain = oracle.layout(idx, cfg.E, cfg.R)
+    al = oracle.layout(idx, cfg.E, cfg.R, expert_alignment=A)
+    cnt = plain["num_tokens_per_expert"]
+    assert np.array_equal(al["num_tokens_per_expert"], cnt)
+    seg = np.diff(al["expert_offset"])
+    assert np.array_equal(seg, (cnt + A - 1) // A * A) and np.all(al["expert_offset"] % A == 0)
+    es, ep_ = al["expert_slot"], plain["expert_slot"]
+    ok = idx >= 0
+    e = np.where(ok, idx, 0)
+    assert np.array_equal(es[ok] - al["expert_offset"][e[ok]], ep_[ok] - plain["expert_offset"][e[ok]])
+    assert np.array_equal(al["rank_slot"], plain["rank_slot"])
+    o = oracle.dispatch(x, idx, w, cfg.E, cfg.R, True, lay=al, with_rank=False)
+    used = np.zeros(o["exp_x"].shape[0], bool)
+    used[es[ok]] = True
+    assert np.all(o["exp_x"][~used] == 0) and np.all(o["exp_scales"][~used] == 0)
+    assert np.all(o["exp_src"][~used] == -1)
+    q, s = oracle.quantize_rows(x)
+    assert np.array_equal(o["exp_x"][used], q[o["exp_src"][used] // cfg.K])
+
+
+def test_two_level_combine():
+    # Level 1: each rank sums its own experts' weighted outputs (one row per
+    # (token, rank)); level 2: the ranks' rows are summed back per token.
+    cfg = _small(3, 300, 256)
+    x, idx, w = _inputs(cfg)
+    lay = oracle.layout(idx, cfg.E, cfg.R)
+    D_e = int(lay["expert_offset"][-1])
+    y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(8, 1), D_e * 256).astype(np.float32)).reshape(D_e, 256)
+    part, st = oracle.combine_to_ranks(y, idx, lay, w, cfg.E, cfg.R)
+    assert st == 0 and part.shape[0] == int(lay["rank_offset"][-1])
+    # each rank row: the f64 sum of that rank's terms, within the fp32 bound and one BF16 rounding
+    L = cfg.E // cfg.R
+    yf = oracle.f32_from_bf16(y).astype(np.float64)
+    pf = oracle.f32_from_bf16(part).astype(np.float64)
+    for t in range(0, cfg.N, 13):
+        for r in range(cfg.R):
+            row = lay["rank_slot"][t, r]
+            if row < 0:
+                continue
+            ks = [k for k in range(cfg.K) if idx[t, k] >= 0 and idx[t, k] // L == r]
+            terms = np.array([w[t, k] * yf[lay["expert_slot"][t, k]] for k in ks])
+            ref = terms.sum(0)
+            bound = len(ks) * 2.0 ** -24 * np.abs(terms).sum(0) + 2.0 ** (
+                np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 8)
+            assert np.all(np.abs(pf[row] - ref) <= bound * 1.0001)
+    out, _ = oracle.combine(part, lay["rank_slot"], None)
+    # with one expert per token the two levels equal the flat combine exactly
+    idx1 = idx[:, :1].copy()
+    lay1 = oracle.layout(idx1, cfg.E, cfg.R)
+    y1 = y[: int(lay1["expert_offset"][-1])]
+    p1, _ = oracle.combine_to_ranks(y1, idx1, lay1, w[:, :1].copy(), cfg.E, cfg.R)
+    o2, _ = oracle.combine(p1, lay1["rank_slot"], None)
+    o1, _ = oracle.combine(y1, lay1["expert_slot"], w[:, :1].copy())
+    assert np.array_equal(o1, o2)
+    # identity experts with weights summing to 1: within two BF16 steps of x
+    o = oracle.dispatch(x, idx, w, cfg.E, cfg.R, False, lay=lay, with_rank=False)
+    part, _ = oracle.combine_to_ranks(o["exp_x"], idx, lay, w, cfg.E, cfg.R)
+    out, _ = oracle.combine(part, lay["rank_slot"], None)
+    xf = oracle.f32_from_bf16(x).astype(np.float64)
+    of = oracle.f32_from_bf16(out).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(xf), 2.0 ** -126))) - 7)
+    assert np.all(np.abs(of - xf) <= 2 * ulp)
