@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--combine-bias", action="store_true", help="add a shared-expert BF16 row in combine")
     ap.add_argument("--combine", default="flat", choices=["flat", "two-level"],
                     help="normal workloads: one weighted sum, or per-rank pre-sums then the cross-rank sum")
+    ap.add_argument("--training", action="store_true",
+                    help="normal workloads: also the backward passes (combine backward, then dispatch backward)")
     ap.add_argument("--ll-combine", default="one-phase", choices=["one-phase", "two-phase"],
                     help="low-latency workloads: combine in one launch, or send + receive hook")
     ap.add_argument("--no-e2e", action="store_true")
@@ -189,7 +191,7 @@ def fp8_flag_word(ep, cfg, scales: str) -> int:
 class NormalWorkload:
     """Layout, dispatch (per-rank + expert-major, BF16 or FP8), combine."""
 
-    def __init__(self, cfg, dev, inp, scales="fp32", align=1, bias=False, two_level=False):
+    def __init__(self, cfg, dev, inp, scales="fp32", align=1, bias=False, two_level=False, training=False):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
@@ -231,6 +233,15 @@ class NormalWorkload:
         else:
             self.y = self.exp_x
         self.phases = ["layout", "dispatch"] + (["combine_to_ranks", "combine_ranks"] if two_level else ["combine"])
+        self.training = training
+        if training:
+            # Backward: a gradient of the combined output flows back through
+            # combine (to the expert rows and the weights), then through dispatch.
+            self.grad_out = torch.empty((N, H), dtype=torch.bfloat16, device=dev).normal_()
+            self.grad_y = torch.empty((cap_e, H), dtype=torch.bfloat16, device=dev)
+            self.grad_w = torch.empty((N, K), dtype=torch.float32, device=dev)
+            self.grad_x = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+            self.phases += ["combine_backward", "dispatch_backward"]
         self.dominant = "dispatch"
         self.kernel_names = {"layout": "layout_kernel", "dispatch": f"dispatch_kernel<{'fp8' if cfg.fp8 else 'bf16'}>",
                              "combine": "combine_kernel", "combine_to_ranks": "combine_to_ranks_kernel",
@@ -263,6 +274,13 @@ class NormalWorkload:
         ep.ep_combine(idx_layout, self.y, w, self.out, self.status, stream, bias=self.bias)
         if ev:
             ev[3].record(stream)
+        if self.training:
+            ep.ep_combine_backward(idx_layout, self.grad_out, self.y, w, self.grad_y, self.grad_w, self.status, stream)
+            if ev:
+                ev[4].record(stream)
+            ep.ep_combine(idx_layout, self.grad_y, None, self.grad_x, self.status, stream)
+            if ev:
+                ev[5].record(stream)
 
     def rows(self):
         r = {"per_rank": int(self.lay.rank_offset[-1].item()),
@@ -291,7 +309,12 @@ class NormalWorkload:
                     "combine_to_ranks": D_e * 2 * H + N * K * 12 + N * R * 4 + D_r * 2 * H,
                     "combine_ranks": D_r * 2 * H + N * R * 4 + N * 2 * H + bias_b}
         combine = D_e * 2 * H + N * K * 8 + N * 2 * H + bias_b  # rows + slots/weights read, out written
-        return {"layout": layout, "dispatch": dispatch, "combine": combine}
+        out = {"layout": layout, "dispatch": dispatch, "combine": combine}
+        if self.training:
+            # grad_out and the forward rows read, grad rows and grad_w written
+            out["combine_backward"] = N * 2 * H + D_e * 2 * H * 2 + N * K * 12
+            out["dispatch_backward"] = D_e * 2 * H + N * K * 4 + N * 2 * H
+        return out
 
 
 class LLWorkload:
@@ -402,7 +425,7 @@ def run_ours(args):
                         bias=args.combine_bias)
     else:
         wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales, align=args.expert_alignment,
-                            bias=args.combine_bias, two_level=args.combine == "two-level")
+                            bias=args.combine_bias, two_level=args.combine == "two-level", training=args.training)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lay = wl.layout_for(wl.idx)
@@ -513,7 +536,7 @@ def run_ours(args):
                    "l2": "flushed between steps (256 MiB write)",
                    "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
                                "combine": args.combine, "ll_combine": args.ll_combine,
-                               "fp8_scales": args.fp8_scales},
+                               "fp8_scales": args.fp8_scales, "training": args.training},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "rows": wl.rows()},
         "phases": phases,

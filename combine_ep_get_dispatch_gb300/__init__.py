@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
         "ep_combine": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P, P]),
         "ep_combine_to_ranks": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, I64, P, P]),
         "ep_combine_ranks": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P]),
+        "ep_combine_backward": (I, [ctypes.POINTER(ep_layout_t), P, P, I64, I, P, P, P, P, P]),
         "ep_ll_workspace_bytes": (SZ, [I, I, I, I, I]),
         "ep_ll_dispatch_send": (I, [P, P, I, I, I, I, I, I, I, P, P, P, P, SZ, P, P]),
         "ep_ll_dispatch_recv": (I, [P, SZ, I, I, I, I, I, P, P, P, P, P]),
@@ -252,6 +253,17 @@ def ep_combine_to_ranks(layout: Layout, expert_y: torch.Tensor, topk_weights: to
                                      _stream(stream)), "ep_combine_to_ranks")
 
 
+def ep_combine_backward(layout: Layout, grad_out: torch.Tensor, expert_y: Optional[torch.Tensor],
+                        topk_weights: torch.Tensor, grad_y: Optional[torch.Tensor], grad_w: Optional[torch.Tensor],
+                        status: Optional[torch.Tensor] = None, stream=None) -> None:
+    c = layout.c_struct()
+    ref = expert_y if expert_y is not None else grad_y
+    rows = ref.shape[0] if ref is not None else 0
+    _check(lib().ep_combine_backward(ctypes.byref(c), _p(grad_out), _p(expert_y), rows, grad_out.shape[1],
+                                     _p(topk_weights), _p(grad_y), _p(grad_w), _p(status), _stream(stream)),
+           "ep_combine_backward")
+
+
 def ep_combine_ranks(layout: Layout, rank_y: torch.Tensor, out: torch.Tensor, status: Optional[torch.Tensor] = None,
                      stream=None, bias: Optional[torch.Tensor] = None) -> None:
     c = layout.c_struct()
@@ -386,6 +398,28 @@ def combine(expert_y: torch.Tensor, layout: Layout, topk_weights: torch.Tensor,
     b = bias.contiguous() if bias is not None else None
     ep_combine(layout, expert_y.contiguous(), topk_weights.contiguous(), out, status, stream, bias=b)
     return out
+
+
+def dispatch_backward(grad_expert_x: torch.Tensor, layout: Layout, status: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """grad_x [N, H] bf16: the unit-weight sum of each token's expert-major row gradients."""
+    N = layout.topk_idx.shape[0]
+    out = torch.empty((N, grad_expert_x.shape[1]), dtype=torch.bfloat16, device=grad_expert_x.device)
+    c = layout.c_struct()
+    g = grad_expert_x.contiguous()
+    _check(lib().ep_combine(ctypes.byref(c), _p(g), g.shape[0], g.shape[1], None, None, _p(out), _p(status),
+                            _stream(stream)), "ep_combine")
+    return out
+
+
+def combine_backward(grad_out: torch.Tensor, layout: Layout, expert_y: torch.Tensor, topk_weights: torch.Tensor,
+                     status: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(grad_y [rows, H] bf16, grad_w [N, K] fp32) of out = sum_k w * expert_y[expert_slot]."""
+    grad_y = torch.zeros_like(expert_y)
+    grad_w = torch.empty_like(topk_weights, dtype=torch.float32)
+    ep_combine_backward(layout, grad_out.contiguous(), expert_y.contiguous(), topk_weights.contiguous(), grad_y,
+                        grad_w, status, stream)
+    return grad_y, grad_w
 
 
 def combine_two_level(expert_y: torch.Tensor, layout: Layout, topk_weights: torch.Tensor,

@@ -216,8 +216,8 @@ int ep_combine(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int h
                const float* topk_weights, const void* bias, void* out, int32_t* status, void* stream) {
   if (!layout_ok(L) || !hidden_ok(hidden, 0) || y_rows < 0) return EP_ERR_INVALID_ARG;
   const int N = L->num_tokens;
-  if (N > 0 && (!L->expert_slot || !topk_weights || !out || (!expert_y && y_rows > 0)))
-    return EP_ERR_INVALID_ARG;
+  // topk_weights may be NULL: a unit-weight sum (the backward of dispatch).
+  if (N > 0 && (!L->expert_slot || !out || (!expert_y && y_rows > 0))) return EP_ERR_INVALID_ARG;
   if (!aligned16(expert_y) || !aligned16(out) || !aligned16(bias)) return EP_ERR_ALIGNMENT;
   CombineParams p{};
   p.y = static_cast<const uint16_t*>(expert_y);
@@ -270,6 +270,28 @@ int ep_combine_ranks(const ep_layout_t* L, const void* rank_y, int64_t rank_rows
   p.N = N; p.K = L->num_ranks; p.H = hidden;
   p.status = status;
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_combine_backward(const ep_layout_t* L, const void* grad_out, const void* expert_y, int64_t y_rows,
+                        int hidden, const float* topk_weights, void* grad_y, float* grad_w, int32_t* status,
+                        void* stream) {
+  if (!layout_ok(L) || !hidden_ok(hidden, 0) || y_rows < 0) return EP_ERR_INVALID_ARG;
+  const int N = L->num_tokens;
+  if (N > 0 && (!L->expert_slot || !grad_out || !topk_weights)) return EP_ERR_INVALID_ARG;
+  if (grad_w && !expert_y && y_rows > 0) return EP_ERR_INVALID_ARG;
+  if (!aligned16(grad_out) || !aligned16(expert_y) || !aligned16(grad_y)) return EP_ERR_ALIGNMENT;
+  if (!grad_y && !grad_w) return EP_OK;
+  CombineBwdParams p{};
+  p.grad_out = static_cast<const uint16_t*>(grad_out);
+  p.y = static_cast<const uint16_t*>(expert_y);
+  p.y_rows = y_rows;
+  p.slot = L->expert_slot;
+  p.w = topk_weights;
+  p.grad_y = static_cast<uint16_t*>(grad_y);
+  p.grad_w = grad_w;
+  p.N = N; p.K = L->num_topk; p.H = hidden;
+  p.status = status;
+  return cuda_rc(launch_combine_backward(p, static_cast<cudaStream_t>(stream)));
 }
 
 size_t ep_ll_workspace_bytes(int N, int K, int E, int R, int T) {

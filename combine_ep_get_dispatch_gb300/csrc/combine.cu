@@ -228,4 +228,92 @@ cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s)
   return cudaGetLastError();
 }
 
+// ---- combine backward --------------------------------------------------------------
+// For out[t] = sum_k w[t,k] y[slot[t,k]]: grad_y[slot[t,k]] = bf16(w[t,k] *
+// grad_out[t]) (the backward of combine is a dispatch of the weighted
+// gradient) and grad_w[t,k] = <grad_out[t], y[slot[t,k]]> in fp32: each
+// thread chains its vectors' products with fused multiply-adds, then a fixed
+// shuffle / shared-memory tree sums the threads, so the result is the same on
+// every run. One block per token.
+__global__ void __launch_bounds__(kThreads) combine_backward_kernel(const CombineBwdParams p) {
+  __shared__ int32_t s_row[EP_MAX_TOPK];
+  __shared__ float s_w[EP_MAX_TOPK];
+  __shared__ float s_red[kThreads / 32][kChunk];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = p.K, H = p.H, nvec = H / 8;
+  for (int64_t t = blockIdx.x; t < p.N; t += gridDim.x) {
+    if (tid < K) {
+      int32_t row = __ldg(p.slot + t * K + tid);
+      if (row >= p.y_rows) {
+        flag(p.status, EP_ST_CAPACITY);
+        row = -1;
+      }
+      s_row[tid] = row;
+      s_w[tid] = __ldg(p.w + t * K + tid);
+    }
+    __syncthreads();
+    const uint4* g_row = reinterpret_cast<const uint4*>(p.grad_out + t * H);
+    for (int k0 = 0; k0 < K; k0 += kChunk) {
+      float dot[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) dot[j] = 0.0f;
+      for (int v = tid; v < nvec; v += kThreads) {
+        const uint4 g = __ldg(g_row + v);
+        const float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                             bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          const int k = k0 + j;
+          const int32_t row = (k < K) ? s_row[k] : -1;
+          if (row < 0) continue;
+          if (p.grad_y) {
+            const float wk = s_w[k];
+            uint4 o;
+            o.x = pack_bf16x2(__fmul_rn(wk, gf[0]), __fmul_rn(wk, gf[1]));
+            o.y = pack_bf16x2(__fmul_rn(wk, gf[2]), __fmul_rn(wk, gf[3]));
+            o.z = pack_bf16x2(__fmul_rn(wk, gf[4]), __fmul_rn(wk, gf[5]));
+            o.w = pack_bf16x2(__fmul_rn(wk, gf[6]), __fmul_rn(wk, gf[7]));
+            reinterpret_cast<uint4*>(p.grad_y + static_cast<int64_t>(row) * H)[v] = o;
+          }
+          if (p.grad_w && p.y) {
+            const uint4 yv = __ldg(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
+            dot[j] = __fmaf_rn(gf[0], bf16_lo(yv.x), dot[j]);
+            dot[j] = __fmaf_rn(gf[1], bf16_hi(yv.x), dot[j]);
+            dot[j] = __fmaf_rn(gf[2], bf16_lo(yv.y), dot[j]);
+            dot[j] = __fmaf_rn(gf[3], bf16_hi(yv.y), dot[j]);
+            dot[j] = __fmaf_rn(gf[4], bf16_lo(yv.z), dot[j]);
+            dot[j] = __fmaf_rn(gf[5], bf16_hi(yv.z), dot[j]);
+            dot[j] = __fmaf_rn(gf[6], bf16_lo(yv.w), dot[j]);
+            dot[j] = __fmaf_rn(gf[7], bf16_hi(yv.w), dot[j]);
+          }
+        }
+      }
+      if (p.grad_w) {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          float d = dot[j];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          if (lane == 0) s_red[warp][j] = d;
+        }
+        __syncthreads();
+        if (tid < kChunk && k0 + tid < K) {
+          float d = 0.0f;
+          for (int ww = 0; ww < kThreads / 32; ++ww) d += s_red[ww][tid];
+          p.grad_w[t * K + k0 + tid] = (s_row[k0 + tid] >= 0 && p.y) ? d : 0.0f;
+        }
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s) {
+  if (p.N <= 0) return cudaSuccess;
+  const int64_t cap = int64_t(1) << 30;
+  combine_backward_kernel<<<static_cast<int>(p.N < cap ? p.N : cap), kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace ep

@@ -94,6 +94,18 @@ struct CombineRanksParams {
   int32_t* status;
 };
 
+struct CombineBwdParams {
+  const uint16_t* grad_out;  // [N, H]
+  const uint16_t* y;         // [y_rows, H] forward expert outputs, or null (no grad_w)
+  int64_t y_rows;
+  const int32_t* slot;       // [N, K]
+  const float* w;            // [N, K]
+  uint16_t* grad_y;          // [y_rows, H] or null
+  float* grad_w;             // [N, K] or null
+  int N, K, H;
+  int32_t* status;
+};
+
 struct PadParams {
   const int32_t* expert_off;   // [E+1] aligned offsets
   const int32_t* per_expert;   // [E] true counts
@@ -126,6 +138,7 @@ cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll,
 cudaError_t launch_dispatch(const DispatchParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s);
+cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s);
 cudaError_t launch_pad_zero(const PadParams& p, cudaStream_t s);
 cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);

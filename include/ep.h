@@ -248,7 +248,10 @@ int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags,
  *   y_rows        rows of expert_y; slots at or beyond it are skipped and
  *                 flagged EP_ST_CAPACITY
  *   hidden        a multiple of 8, <= EP_MAX_HIDDEN
- *   topk_weights  [N, K] fp32 router weights
+ *   topk_weights  [N, K] fp32 router weights, or NULL for unit weights: the
+ *                 unweighted sum of a token's expert-major rows is the
+ *                 backward of dispatch ("DeepEP V1 (legacy) guide", section
+ *                 5.1: the backward of dispatch is a combine)
  *   bias          [N, hidden] BF16 or NULL: added in fp32 after the weighted
  *                 sum, before the BF16 rounding (the shared expert's output
  *                 folded into the epilogue, "DeepEP Ascend deep dive",
@@ -289,6 +292,25 @@ int ep_combine_to_ranks(const ep_layout_t* L, const void* expert_y, int64_t y_ro
  */
 int ep_combine_ranks(const ep_layout_t* L, const void* rank_y, int64_t rank_rows, int hidden,
                      const void* bias, void* out, int32_t* status, void* stream);
+
+/*
+ * Backward of combine ("DeepEP V1 (legacy) guide", section 5.1: the backward
+ * of combine is a dispatch). For out[t] = sum_k w[t, k] y[expert_slot[t, k]]:
+ *   grad_y[expert_slot[t, k]] = bf16( w[t, k] * grad_out[t] )   (fp32 product)
+ *   grad_w[t, k]              = <grad_out[t], y[expert_slot[t, k]]>, fp32, in a
+ *                               fixed order (deterministic), 0 for masked slots
+ * The gradient of a combine bias is grad_out itself.
+ *
+ *   grad_out      [N, hidden] BF16
+ *   expert_y      [y_rows, hidden] BF16 forward expert outputs (needed for grad_w)
+ *   topk_weights  [N, K] fp32
+ *   grad_y        [y_rows, hidden] BF16, or NULL to skip; rows that no slot
+ *                 names (padding, capacity slack) are not written
+ *   grad_w        [N, K] fp32, or NULL to skip
+ */
+int ep_combine_backward(const ep_layout_t* L, const void* grad_out, const void* expert_y, int64_t y_rows,
+                        int hidden, const float* topk_weights, void* grad_y, float* grad_w,
+                        int32_t* status, void* stream);
 
 /*
  * Bytes of device workspace the low-latency calls need. The workspace

@@ -56,6 +56,8 @@ def lib():
         L.oracle_combine.argtypes = [P, i64, P, P, P, i32, i32, i32, P]
         L.oracle_combine_to_ranks.argtypes = [P, i64, P, P, P, P, i32, i32, i32, i32, i32, P, i64]
         L.oracle_combine_to_ranks.restype = i32
+        L.oracle_combine_backward.argtypes = [P, P, i64, P, P, i32, i32, i32, P, P]
+        L.oracle_combine_backward.restype = i32
         L.oracle_combine.restype = i32
         L.oracle_ll_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32,
                                          P, P, P, P, P, P]
@@ -272,3 +274,18 @@ def ll_combine_recv(staging: np.ndarray, slot_map: np.ndarray, topk_weights: np.
     out = np.empty((N, H), np.uint16)
     lib().oracle_combine_staged(_p(st_), _p(slot), _p(w), N, K, H, _p(out))
     return out
+
+
+def combine_backward(grad_out: np.ndarray, y_bf16: np.ndarray, slot: np.ndarray,
+                     topk_weights: np.ndarray) -> tuple:
+    """(grad_y [rows, H] BF16 bits, grad_w [N, K] float64) of out = sum_k w * y[slot]."""
+    g = np.ascontiguousarray(grad_out, dtype=np.uint16)
+    y = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    slot = np.ascontiguousarray(slot, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    N, K = slot.shape
+    H = g.shape[1]
+    grad_y = np.zeros(y.shape, np.uint16)
+    grad_w = np.empty((N, K), np.float64)
+    st = lib().oracle_combine_backward(_p(g), _p(y), y.shape[0], _p(slot), _p(w), N, K, H, _p(grad_y), _p(grad_w))
+    return grad_y, grad_w, int(st)

@@ -338,6 +338,36 @@ int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const
   return status;
 }
 
+// Combine backward (training reuse, "DeepEP V1 (legacy) guide" 5.1: the
+// backward of combine is a dispatch). For out[t] = sum_k w[t,k] y[slot[t,k]]:
+//   grad_y[slot[t,k]] = bf16( w[t,k] * grad_out[t] )          (fp32 product)
+//   grad_w[t,k]       = sum_h grad_out[t,h] * y[slot[t,k],h]  (double here;
+//                        the library's fp32 sum is checked within its bound)
+// Masked slots get nothing (grad_w = 0).
+int oracle_combine_backward(const uint16_t* grad_out, const uint16_t* y, int64_t y_rows, const int32_t* slot,
+                            const float* w, int N, int K, int H, uint16_t* grad_y, double* grad_w) {
+  int status = 0;
+  for (int t = 0; t < N; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int64_t tk = static_cast<int64_t>(t) * K + k;
+      const int32_t row = slot[tk];
+      if (grad_w) grad_w[tk] = 0.0;
+      if (row < 0) continue;
+      if (row >= y_rows) { status |= kCapacity; continue; }
+      const uint16_t* g = grad_out + static_cast<int64_t>(t) * H;
+      if (grad_y)
+        for (int h = 0; h < H; ++h)
+          grad_y[static_cast<int64_t>(row) * H + h] = bf16_from_f32(w[tk] * f32_from_bf16(g[h]));
+      if (grad_w && y) {
+        double acc = 0.0;
+        for (int h = 0; h < H; ++h)
+          acc += static_cast<double>(f32_from_bf16(g[h])) * f32_from_bf16(y[static_cast<int64_t>(row) * H + h]);
+        grad_w[tk] = acc;
+      }
+    }
+  return status;
+}
+
 // Two-level combine, first level (the expert layer's reduction on each rank,
 // as in DeepEP's normal combine(x, handle), "DeepEP V1 (legacy) guide" 5.1):
 // for every (t, r) in the mask, rank_out[rank_slot[t,r]] = bf16( sum over k

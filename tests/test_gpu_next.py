@@ -256,3 +256,38 @@ def test_two_level_combine_matches_oracle():
     want, _ = oracle.combine(part, lay_ref["rank_slot"], None, bias)
     assert np.array_equal(u16(out), want)
     assert status_value(st) == 0
+
+
+def test_dispatch_and_combine_backward():
+    cfg = ei.CONFIGS[4].scaled(N=700, H=2048)
+    d = ei.make_inputs(cfg, seed=100)
+    idx, w = d["topk_idx"], d["topk_weights"]
+    lay_ref = oracle.layout(idx, cfg.E, cfg.R)
+    es = lay_ref["expert_slot"]
+    D_e = int(lay_ref["expert_offset"][-1])
+    st = _status()
+    lay = ep.get_dispatch_layout(to_dev(idx), cfg.E, cfg.R, status=st)
+    # dispatch backward: unit-weight sum of the row gradients
+    g_rows = _expert_outputs((D_e, cfg.H), seed=101)
+    gx = ep.dispatch_backward(to_dev_bf16(g_rows), lay, status=st)
+    want, _ = oracle.combine(g_rows, es, None)
+    assert np.array_equal(u16(gx), want)
+    # combine backward
+    y = _expert_outputs((D_e, cfg.H), seed=102)
+    g = _expert_outputs((cfg.N, cfg.H), seed=103)
+    gy, gw = ep.combine_backward(to_dev_bf16(g), lay, to_dev_bf16(y), to_dev(w), status=st)
+    ref_gy, ref_gw, _ = oracle.combine_backward(g, y, es, w)
+    assert np.array_equal(u16(gy), ref_gy)
+    gw = gw.cpu().numpy().astype(np.float64)
+    gf = oracle.f32_from_bf16(g).astype(np.float64)
+    yf = oracle.f32_from_bf16(y).astype(np.float64)
+    bound = np.zeros_like(ref_gw)
+    ok = es >= 0
+    for t, k in zip(*np.nonzero(ok)):
+        bound[t, k] = cfg.H * 2.0 ** -24 * np.abs(gf[t] * yf[es[t, k]]).sum()
+    assert np.all(np.abs(gw - ref_gw) <= bound + 1e-30)
+    assert np.all(gw[~ok] == 0)
+    # deterministic: the same bits on a second run
+    gy2, gw2 = ep.combine_backward(to_dev_bf16(g), lay, to_dev_bf16(y), to_dev(w), status=st)
+    assert torch.equal(gy, gy2) and np.array_equal(gw, gw2.cpu().numpy().astype(np.float64))
+    assert status_value(st) == 0

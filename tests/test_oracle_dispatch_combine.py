@@ -351,3 +351,46 @@ def test_two_level_combine():
     of = oracle.f32_from_bf16(out).astype(np.float64)
     ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(xf), 2.0 ** -126))) - 7)
     assert np.all(np.abs(of - xf) <= 2 * ulp)
+
+
+def test_backward_adjoint_identities():
+    # Training reuse ("DeepEP V1 guide" 5.1): dispatch backward is a combine
+    # with unit weights, combine backward is a dispatch (of the weighted
+    # gradient). Both pinned by adjoint identities and a finite difference,
+    # computed in float64 with numpy, independently of the oracle's code.
+    cfg = _small(3, 120, 256)
+    x, idx, w = _inputs(cfg, seed=6)
+    lay = oracle.layout(idx, cfg.E, cfg.R)
+    es = lay["expert_slot"]
+    D_e = int(lay["expert_offset"][-1])
+    o = oracle.dispatch(x, idx, w, cfg.E, cfg.R, False, lay=lay, with_rank=False)
+    g_rows = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(6, 1), D_e * 256).astype(np.float32)).reshape(D_e, 256)
+    # <dispatch(x), g> == <x, dispatch_backward(g)>: dispatch_backward = unit-weight combine
+    gx, _ = oracle.combine(g_rows, es, None)
+    f = lambda a: oracle.f32_from_bf16(a).astype(np.float64)
+    lhs = (f(o["exp_x"]) * f(g_rows)).sum()
+    ref_gx = np.zeros((cfg.N, 256))
+    ok = es >= 0
+    for t, k in zip(*np.nonzero(ok)):
+        ref_gx[t] += f(g_rows)[es[t, k]]
+    assert abs(lhs - (f(x) * ref_gx).sum()) <= 1e-9 * np.abs(f(x) * ref_gx).sum()
+    assert np.all(np.abs(f(gx) - ref_gx) <= np.abs(ref_gx) * 2.0 ** -7 + 1e-30 + cfg.K * 2.0 ** -24 * np.abs(ref_gx))
+    # combine backward: grad_y rows are bf16(w * g); grad_w is the finite difference of <g, combine(y, w)>
+    y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(6, 2), D_e * 256).astype(np.float32)).reshape(D_e, 256)
+    g = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(6, 3), cfg.N * 256).astype(np.float32)).reshape(cfg.N, 256)
+    gy, gw, st = oracle.combine_backward(g, y, es, w)
+    assert st == 0
+    for t, k in list(zip(*np.nonzero(ok)))[::17]:
+        want = ei.bf16_bits_from_f32((w[t, k] * oracle.f32_from_bf16(g[t])).astype(np.float32))
+        assert np.array_equal(gy[es[t, k]], want)
+
+        def loss(wtk):
+            out = np.zeros(256)
+            for kk in range(cfg.K):
+                if es[t, kk] >= 0:
+                    out += (wtk if kk == k else float(w[t, kk])) * f(y)[es[t, kk]]
+            return (f(g)[t] * out).sum()
+        d = 0.25
+        fd = (loss(float(w[t, k]) + d) - loss(float(w[t, k]) - d)) / (2 * d)   # exact: loss is linear in w
+        assert abs(gw[t, k] - fd) <= 1e-9 * (1 + abs(fd))
+    assert np.all(gw[~ok] == 0)
