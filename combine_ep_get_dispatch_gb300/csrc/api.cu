@@ -10,7 +10,7 @@ namespace {
 using namespace ep;
 
 constexpr int kVersion = 100;  // 0.1.0
-constexpr int64_t kEntriesPerCta = 6144;
+constexpr int64_t kEntriesPerCta = 1024;  // (token, slot) entries per layout CTA (measured)
 constexpr int kMaxLayoutCtas = 256;
 
 inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }

@@ -18,9 +18,10 @@
 // (cp.async.bulk shared->global) issued by the lane that owns that
 // destination, so the copy engine generates the addresses and the SM issues
 // ~R'+K' instructions per token. Grid: persistent, a multiple of the SM count.
-// FP8: a register path (see dispatch_fp8_kernel below): quantisation needs
-// the SM anyway, and without the BF16 staging buffers five times more warps
-// fit on an SM.
+// FP8: registers in, bulk TMA out (see dispatch_fp8_kernel below): the warp
+// quantises its token's row into shared memory and each destination row is
+// again one bulk store, so the row loads do not queue behind a flood of
+// register stores in the SM's load/store path.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -152,22 +153,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
   bulk_wait<0>();
 }
 
-// ---- FP8 dispatch: register path ---------------------------------------------
+// ---- FP8 dispatch ---------------------------------------------------------------
 // A warp per token. Lanes own 16 consecutive channels of a 512-channel step
-// (8 lanes = one 128-channel block): two 16-byte loads of BF16, a shuffle max
-// over the block, the IEEE division by the scale, 16 E4M3 codes packed into
-// one 16-byte store per destination row. Shared memory holds only the
-// token's destination list and its scales, so up to 40 warps share an SM and
-// hide the quantisation latency. (Measured against staging the E4M3 row in
-// shared memory and writing it with bulk TMA stores, which was slower here.)
-constexpr int kF8Threads = 256;
+// (8 lanes = one 128-channel block): two 16-byte loads of BF16 (issued one
+// step ahead), a shuffle max over the block, the IEEE division by the scale,
+// 16 E4M3 codes into the warp's shared-memory row. Once the row is complete,
+// each destination row is one bulk store (cp.async.bulk shared->global)
+// issued by the lane that owns it, and the scales follow with plain stores
+// (a UE8M0 scale row is not a multiple of 16 bytes). Measured on GB300
+// against 16-byte register stores to every destination (the loads then wait
+// behind the stores) and against a block per token.
+constexpr int kF8Threads = 128;
 constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank copies
-
-struct F8Warp {
-  uint8_t* xdst[kF8MaxDest];
-  void* sdst[kF8MaxDest];
-  float scales[EP_MAX_HIDDEN / 128];
-};
 
 // Smallest power of two >= s for s >= 0 (exact on the bit pattern; a
 // subnormal m * 2^-149 rounds to the next power of two of m).
@@ -219,17 +216,33 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
   return q;
 }
 
+// Shared memory of one warp: the token's E4M3 row (H bytes, the source of
+// the bulk stores), its H/128 scales and its destination rows (expert-major
+// rows first, then per-rank rows).
+__host__ __device__ inline unsigned f8_warp_bytes(int H) {
+  return round_up(static_cast<unsigned>(H) + static_cast<unsigned>(H / 128) * 4u + kF8MaxDest * 4u, 128u);
+}
+
 __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const DispatchParams p) {
-  __shared__ F8Warp sw[kF8Threads / 32];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  F8Warp& me = sw[w];
   const int H = p.H, K = p.K, R = p.R, L = p.L, E = p.E;
-  const int64_t nsc = H / 128;
+  const int nsc = H / 128;
+  uint8_t* row = smem + static_cast<size_t>(w) * f8_warp_bytes(H);
+  float* scales = reinterpret_cast<float*>(row + H);
+  int32_t* drow = reinterpret_cast<int32_t*>(scales + nsc);
   const bool ue8m0 = p.fp8_flags & EP_FP8_UE8M0;
-  const int64_t ssz = ue8m0 ? 1 : 4;  // bytes per scale
   const int64_t N = p.N;
   const int64_t nw = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + w; t < N; t += nw) {
+    const uint16_t* xr = p.x + t * H;
+    // The first step's channels are requested before the destination
+    // lookups, and each step requests the next one's before it quantises.
+    uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
+    if (lane * 16 < H) {
+      n0 = ld_nc_v4(xr + lane * 16);
+      n1 = ld_nc_v4(xr + lane * 16 + 8);
+    }
     // Destinations: expert-major rows (lane k < K), then per-rank rows.
     int e_k = -1;
     float w_k = 0.0f;
@@ -248,13 +261,9 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
       }
     }
     const unsigned vm = __ballot_sync(0xffffffffu, erow >= 0);
-    if (erow >= 0) {
-      const int pos = __popc(vm & lanemask_lt());
-      me.xdst[pos] = p.exp_x + static_cast<int64_t>(erow) * H;
-      me.sdst[pos] = p.exp_scales ? static_cast<uint8_t*>(p.exp_scales) + static_cast<int64_t>(erow) * nsc * ssz
-                                  : nullptr;
-    }
-    int n = __popc(vm);
+    if (erow >= 0) drow[__popc(vm & lanemask_lt())] = erow;
+    const int ne = __popc(vm);
+    int n = ne;
     if (p.rank_x) {
       for (int rb = 0; rb < R; rb += 32) {
         const int r = rb + lane;
@@ -267,12 +276,7 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
         // at most K ranks hold a copy of one token; the list has room for K more
         if (rrow >= 0) {
           const int pos = n + __popc(rm & lanemask_lt());
-          if (pos < kF8MaxDest) {
-            me.xdst[pos] = p.rank_x + static_cast<int64_t>(rrow) * H;
-            me.sdst[pos] = p.rank_scales
-                               ? static_cast<uint8_t*>(p.rank_scales) + static_cast<int64_t>(rrow) * nsc * ssz
-                               : nullptr;
-          }
+          if (pos < kF8MaxDest) drow[pos] = rrow;
           if (p.rank_src) p.rank_src[rrow] = static_cast<int32_t>(t);
         }
         n = min(n + __popc(rm), kF8MaxDest);
@@ -289,51 +293,62 @@ __global__ void __launch_bounds__(kF8Threads) dispatch_fp8_kernel(const Dispatch
         }
       }
     }
-    __syncwarp();
 
-    // Quantise and store, 512 channels per step. (Loading several steps
-    // ahead was measured: the extra registers cost more warps than the
-    // deeper loads gained.)
-    const uint16_t* xr = p.x + t * H;
+    // Quantise into the shared row, 512 channels per step.
     for (int c0 = 0; c0 < H; c0 += 512) {
       const int c = c0 + lane * 16;
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (c < H) {
-        v0 = __ldg(reinterpret_cast<const uint4*>(xr + c));
-        v1 = __ldg(reinterpret_cast<const uint4*>(xr + c + 8));
+      const uint4 v0 = n0, v1 = n1;
+      if (c + 512 < H) {
+        n0 = ld_nc_v4(xr + c + 512);
+        n1 = ld_nc_v4(xr + c + 512 + 8);
       }
       float sc;
       const uint4 q = quantize16(v0, v1, sc, p.fp8_flags);
+      if (c0 == 0) {
+        bulk_wait_read<0>();  // the previous token's stores have read the row
+        __syncwarp();
+      }
       if (c < H) {
-        if ((lane & 7) == 0) me.scales[c >> 7] = sc;
-        for (int d = 0; d < n; ++d) st_v4(me.xdst[d] + c, q);
+        *reinterpret_cast<uint4*>(row + c) = q;
+        if ((lane & 7) == 0) scales[c >> 7] = sc;
       }
     }
+    fence_proxy_async_smem();
     __syncwarp();
+    // One bulk store per destination row; lane d issues row d.
+    for (int d = lane; d < n; d += 32) {
+      uint8_t* base = d < ne ? p.exp_x : p.rank_x;
+      bulk_s2g(base + static_cast<int64_t>(drow[d]) * H, row, static_cast<unsigned>(H));
+    }
+    bulk_commit();
     for (int d = 0; d < n; ++d) {
-      void* sd = me.sdst[d];
-      if (!sd) continue;
+      void* sbase = d < ne ? p.exp_scales : p.rank_scales;
+      if (!sbase) continue;
+      const int64_t r0 = static_cast<int64_t>(drow[d]) * nsc;
       if (ue8m0)
-        for (int64_t b = lane; b < nsc; b += 32) static_cast<uint8_t*>(sd)[b] = ue8m0_byte(me.scales[b]);
+        for (int b = lane; b < nsc; b += 32) static_cast<uint8_t*>(sbase)[r0 + b] = ue8m0_byte(scales[b]);
       else
-        for (int64_t b = lane; b < nsc; b += 32) static_cast<float*>(sd)[b] = me.scales[b];
+        for (int b = lane; b < nsc; b += 32) static_cast<float*>(sbase)[r0 + b] = scales[b];
     }
     __syncwarp();
   }
+  bulk_wait<0>();
 }
 
+// One warp per token and no persistent loop: a block retires as soon as its
+// four rows have been read out, and the next block takes its place (measured
+// faster than a persistent grid, whose warps wait on their previous token's
+// stores before reusing the staged row).
 cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel, kF8Threads, 0);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int wpb = kF8Threads / 32;
-  const int64_t need = (p.N + wpb - 1) / wpb;
-  const int64_t full = static_cast<int64_t>(per_sm) * sms;
-  dispatch_fp8_kernel<<<static_cast<int>(need < full ? need : full), kF8Threads, 0, s>>>(p);
+  const size_t smem = static_cast<size_t>(wpb) * f8_warp_bytes(p.H);
+  const void* fn = reinterpret_cast<const void*>(&dispatch_fp8_kernel);
+  const cudaError_t err =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int64_t grid = (p.N + wpb - 1) / wpb;
+  dispatch_fp8_kernel<<<static_cast<unsigned>(grid), kF8Threads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
