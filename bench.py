@@ -16,7 +16,8 @@ identity expert outputs (the expert-major rows) back into [16384, 7168] BF16.
 Prints one JSON line (rank 0). `value` is tokens/s of the whole job with
 inputs resident in HBM; `e2e` is the same through the C ABI from pinned host
 buffers, with the host->device copy of x / topk_idx / topk_weights and the
-device->host copy of the combined output inside the timed region.
+device->host copy of the combined output of every step inside the timed
+region (pipelined: a step's copies overlap its neighbours' compute).
 
 --impl reference times the CPU oracle (plain single-threaded C++) on the same
 workload, each step a bounded sample of tokens.
@@ -253,8 +254,9 @@ class NormalWorkload:
                               L.is_token_in_rank, L.rank_offset, L.expert_offset, L.rank_slot, L.expert_slot,
                               L.expert_alignment)
 
-    def run(self, stream, x, idx_layout, w, ev=None):
+    def run(self, stream, x, idx_layout, w, ev=None, out=None):
         ep = self.ep
+        out = self.out if out is None else out
         if ev:
             ev[0].record(stream)
         ep.ep_get_dispatch_layout(idx_layout, self.ws, self.status, stream)
@@ -267,11 +269,11 @@ class NormalWorkload:
             ep.ep_combine_to_ranks(idx_layout, self.y, w, self.rank_y, self.status, stream)
             if ev:
                 ev[3].record(stream)
-            ep.ep_combine_ranks(idx_layout, self.rank_y, self.out, self.status, stream, bias=self.bias)
+            ep.ep_combine_ranks(idx_layout, self.rank_y, out, self.status, stream, bias=self.bias)
             if ev:
                 ev[4].record(stream)
             return
-        ep.ep_combine(idx_layout, self.y, w, self.out, self.status, stream, bias=self.bias)
+        ep.ep_combine(idx_layout, self.y, w, out, self.status, stream, bias=self.bias)
         if ev:
             ev[3].record(stream)
         if self.training:
@@ -362,8 +364,9 @@ class LLWorkload:
     def layout_for(self, idx):
         return idx
 
-    def run(self, stream, x, idx, w, ev=None):
+    def run(self, stream, x, idx, w, ev=None, out=None):
         ep, c = self.ep, self.cfg
+        out = self.out if out is None else out
         if ev:
             ev[0].record(stream)
         ep.ep_ll_dispatch_send(x, idx, c.H, c.E, c.R, c.T, self.flags, self.recv_x, self.recv_s, self.recv_src,
@@ -378,12 +381,12 @@ class LLWorkload:
             ep.ep_ll_combine_send(self.y, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.staging, self.status, stream)
             if ev:
                 ev[3].record(stream)
-            ep.ep_ll_combine_recv(self.staging, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status,
+            ep.ep_ll_combine_recv(self.staging, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, out, self.status,
                                   stream, bias=self.bias)
             if ev:
                 ev[4].record(stream)
             return
-        ep.ep_ll_combine(self.y, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, self.out, self.status, stream,
+        ep.ep_ll_combine(self.y, w, self.ws, c.N, c.K, c.H, c.E, c.R, c.T, out, self.status, stream,
                          bias=self.bias)
         if ev:
             ev[3].record(stream)
@@ -457,35 +460,59 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {st}: {ep.ep_error_string(st)}")
 
-    # End to end through the C ABI from pinned host memory.
+    # End to end through the C ABI from pinned host memory, pipelined as a
+    # serving loop runs it: while step i computes, step i+1's inputs go up on
+    # one stream and step i-1's output comes down on another (two sets of
+    # device inputs and outputs; events order the reuse of each set).
     e2e = None
     if not args.no_e2e:
         xp, ip, wp = wl.x_host.pin_memory(), wl.idx_host.pin_memory(), wl.w_host.pin_memory()
-        outp = torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory()
-        xd, idd, wd = torch.empty_like(wl.x), torch.empty_like(wl.idx), torch.empty_like(wl.w)
-        lay_d = wl.layout_for(idd)
+        outp = [torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        xd = [torch.empty_like(wl.x) for _ in range(2)]
+        idd = [torch.empty_like(wl.idx) for _ in range(2)]
+        wd = [torch.empty_like(wl.w) for _ in range(2)]
+        outd = [torch.empty_like(wl.out) for _ in range(2)]
+        lay_d = [wl.layout_for(t) for t in idd]
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         e2e_steps = max(3, min(args.steps, 50))
+        n_all = 2 + e2e_steps
+        up_done = [torch.cuda.Event() for _ in range(n_all)]
+        comp_done = [torch.cuda.Event() for _ in range(n_all)]
+        down_done = [torch.cuda.Event() for _ in range(n_all)]
 
-        def e2e_step():
-            xd.copy_(xp, non_blocking=True)
-            idd.copy_(ip, non_blocking=True)
-            wd.copy_(wp, non_blocking=True)
-            wl.run(stream, xd, lay_d, wd)
-            outp.copy_(wl.out, non_blocking=True)
+        def e2e_step(i):
+            j = i & 1
+            if i >= 2:
+                s_up.wait_event(comp_done[i - 2])      # step i-2 has consumed input set j
+            with torch.cuda.stream(s_up):
+                xd[j].copy_(xp, non_blocking=True)
+                idd[j].copy_(ip, non_blocking=True)
+                wd[j].copy_(wp, non_blocking=True)
+            up_done[i].record(s_up)
+            stream.wait_event(up_done[i])
+            if i >= 2:
+                stream.wait_event(down_done[i - 2])    # output set j has been read back
+            wl.run(stream, xd[j], lay_d[j], wd[j], out=outd[j])
+            comp_done[i].record(stream)
+            s_down.wait_event(comp_done[i])
+            with torch.cuda.stream(s_down):
+                outp[j].copy_(outd[j], non_blocking=True)
+            down_done[i].record(s_down)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        e0.record(s_up)
+        for i in range(2, n_all):
+            e2e_step(i)
+        stream.wait_event(down_done[n_all - 1])
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if not torch.equal(outp, wl.out.cpu()):
+        if not torch.equal(outp[(n_all - 1) & 1], wl.out.cpu()):
             raise RuntimeError("e2e output differs from the device-resident run")
-        e2e = (e2e_ms, xp.numel() * 2 + ip.numel() * 4 + wp.numel() * 4, outp.numel() * 2)
+        e2e = (e2e_ms, xp.numel() * 2 + ip.numel() * 4 + wp.numel() * 4, outp[0].numel() * 2)
     sampler.stop()
 
     total_ms, e2e_ms_max = max_over_ranks([total_ms, e2e[0] if e2e else 0.0], dev, world)
