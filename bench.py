@@ -207,7 +207,7 @@ class NormalWorkload:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         # Buffers allocated once (worst-case capacities: no host sync in a step).
         self.lay = ep.new_layout(self.idx, E, R, self.align)
-        self.ws = torch.empty(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device=dev)
         cap_r, cap_e = N * min(K, R), N * K + E * (self.align - 1)
         xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
         S = H // 128
@@ -334,7 +334,7 @@ class LLWorkload:
         self.w_host = torch.from_numpy(inp["topk_weights"])
         self.x, self.idx, self.w = self.x_host.to(dev), self.idx_host.to(dev), self.w_host.to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws = torch.empty(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device=dev)
         xdt = torch.uint8 if cfg.fp8 else torch.bfloat16
         self.recv_x = torch.empty((E, R * T, H), dtype=xdt, device=dev)
         self.recv_s = torch.empty((E, R * T, H // 128), dtype=torch.uint8 if scales == "ue8m0" else torch.float32,

@@ -42,6 +42,7 @@ EP_ST_LL_OVERFLOW = 0x4
 EP_ST_TIMEOUT = 0x8
 EP_ST_NOT_SENT = 0x10
 EP_ST_MISMATCH = 0x20
+EP_ST_WORKSPACE = 0x40
 
 EP_FP8 = 0x1
 EP_FP8_ROUND_SCALE = 0x2
@@ -318,7 +319,9 @@ def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int
     """Counts, is_token_in_rank mask and slots for a [N, K] int32 topk_idx.
 
     expert_alignment A > 1 pads each expert's expert-major segment to a
-    multiple of A rows (dispatch zero-fills the padding rows).
+    multiple of A rows (dispatch zero-fills the padding rows). A workspace
+    passed in must have been zero-filled once when it was allocated (each
+    call leaves it ready for the next); without one, a zeroed one is made.
     """
     topk_idx = topk_idx.to(torch.int32).contiguous()
     N, K = topk_idx.shape
@@ -327,7 +330,7 @@ def get_dispatch_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int
     if need == 0:
         raise EPError("get_dispatch_layout", EP_ERR_INVALID_ARG)
     if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=topk_idx.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=topk_idx.device)
     ep_get_dispatch_layout(layout, workspace, status, stream)
     return layout
 
@@ -477,7 +480,7 @@ def low_latency_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, num_max_dispat
     if need == 0:
         raise EPError("low_latency_dispatch", EP_ERR_INVALID_ARG)
     if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
     recv_x = torch.empty((E, R * T, H), dtype=torch.uint8 if use_fp8 else torch.bfloat16, device=dev)
     recv_scales = torch.empty((E, R * T, H // 128), dtype=torch.uint8 if use_ue8m0 else torch.float32,
                               device=dev) if use_fp8 else None

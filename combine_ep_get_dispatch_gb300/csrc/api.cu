@@ -110,6 +110,7 @@ const char* ep_error_string(int c) {
     if (c & EP_ST_TIMEOUT) return "status: bounded in-kernel wait timed out";
     if (c & EP_ST_NOT_SENT) return "status: low-latency receive/combine without a send";
     if (c & EP_ST_MISMATCH) return "status: low-latency shapes differ from the send";
+    if (c & EP_ST_WORKSPACE) return "status: workspace barrier words not zero on entry (zero-fill it)";
   }
   return "unknown code";
 }

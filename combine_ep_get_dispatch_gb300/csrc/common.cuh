@@ -126,15 +126,21 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 }
 
 // ---- grid-wide barrier (cooperative launches only) --------------------------
-// `counter` is zero before the launch; the i-th barrier waits for i * gridDim.x
-// arrivals. Bounded: on expiry it flags EP_ST_TIMEOUT and lets the block go on.
-__device__ __forceinline__ void grid_barrier(unsigned* counter, unsigned target, int32_t* status) {
+// One barrier per launch over two words that are zero when the launch
+// starts: bar[0] counts arrivals, bar[1] departures. The last block to leave
+// sets both back to zero (every block has stopped reading bar[0] by then),
+// so the next launch finds them cleared without a separate reset. A block
+// whose arrival count comes back >= nblocks found non-zero words (a
+// workspace that was never zero-filled, or one a timed-out launch left
+// behind): it flags EP_ST_WORKSPACE. The wait is bounded: on expiry it flags
+// EP_ST_TIMEOUT and lets the block go on.
+__device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, int32_t* status) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(counter, 1u);
+    if (atomicAdd(&bar[0], 1u) >= nblocks) flag(status, EP_ST_WORKSPACE);
     unsigned spins = 0;
-    while (ld_acquire_u32(counter) < target) {
+    while (ld_acquire_u32(&bar[0]) < nblocks) {
       if (++spins > kSpinLimit) {
         flag(status, EP_ST_TIMEOUT);
         break;
@@ -142,6 +148,10 @@ __device__ __forceinline__ void grid_barrier(unsigned* counter, unsigned target,
       __nanosleep(64);
     }
     __threadfence();
+    if (atomicAdd(&bar[1], 1u) == nblocks - 1) {
+      atomicExch(&bar[0], 0u);
+      atomicExch(&bar[1], 0u);
+    }
   }
   __syncthreads();
 }

@@ -418,10 +418,6 @@ cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll,
   }
   err = prepare(dev, with_rank, ll, staged);
   if (err != cudaSuccess) return err;
-  if (G > 1) {
-    err = cudaMemsetAsync(p.ws_barrier, 0, sizeof(unsigned), s);
-    if (err != cudaSuccess) return err;
-  }
   LayoutParams q = p;
   q.magic_L = p.L > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + p.L - 1) / p.L) : 0u;
   q.magic_K = p.K > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + p.K - 1) / p.K) : 0u;

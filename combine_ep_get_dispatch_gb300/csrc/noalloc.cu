@@ -12,9 +12,11 @@
 //
 // The array costs every GPU that loads the library kStaticScratchBytes of
 // memory until the process exits. Every call shares it and it keeps the last
-// call's contents; the launch clears the barrier word it needs (the counters
-// are rewritten in full). Calls that overlap on the GPU (for example on two
-// streams without ordering between them) race on it.
+// call's contents; each call zeroes the barrier words first (the layout's
+// own calls leave them zero, but a caller of this entry point cannot clear
+// the array after a timed-out call), and the counters are rewritten in full.
+// Calls that overlap on the GPU (for example on two streams without ordering
+// between them) race on it.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,5 +61,7 @@ extern "C" int ep_get_dispatch_layout_noalloc(const ep_layout_t* L, int32_t* sta
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != EP_OK) return rc;
+  // The layout workspace starts with its 256-byte barrier block.
+  if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return EP_ERR_CUDA;
   return ep_get_dispatch_layout(L, scratch, kStaticScratchBytes, status, stream);
 }

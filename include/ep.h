@@ -61,6 +61,7 @@ extern "C" {
 #define EP_ST_TIMEOUT 0x8     /* a bounded in-kernel wait gave up */
 #define EP_ST_NOT_SENT 0x10   /* low-latency receive without a matching send */
 #define EP_ST_MISMATCH 0x20   /* low-latency shapes differ from those of the send */
+#define EP_ST_WORKSPACE 0x40  /* the workspace's barrier words were not zero on entry */
 
 /* ---- dispatch payload flags (the `fp8_flags` / `use_fp8` arguments) -------
  * 0: BF16 rows. EP_FP8: E4M3 rows with one fp32 scale per 128 channels,
@@ -172,11 +173,16 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, 
  *
  *   L          handle: sizes, topk_idx and the output arrays (see ep_layout_t)
  *   workspace  device scratch of at least ep_layout_workspace_bytes(...)
- *              bytes; its contents on entry do not matter (the call resets
- *              what it needs). Must not be used by another call in flight.
+ *              bytes, zero-filled before its first use (cudaMemset once at
+ *              allocation). Every call leaves it as it needs to find it
+ *              next time, so it is not cleared again between calls. Must
+ *              not be used by another call in flight.
  *   status     EP_ST_BAD_INDEX when an index lies outside [-1, E) (the slot
  *              is treated as -1); EP_ST_TIMEOUT if an internal grid-wide wait
- *              gave up (outputs then invalid).
+ *              gave up; EP_ST_WORKSPACE if the workspace was not zero-filled
+ *              before its first use (or a previous call on it timed out).
+ *              After either of the last two the outputs are invalid and the
+ *              workspace must be zero-filled again.
  * Runs as one cooperative launch.
  */
 int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes,
@@ -201,7 +207,7 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
  * The first call on a device looks up that array's device address (once per
  * device, with the device current); make that first call before any stream
  * capture. Every call shares the array and it keeps the last call's contents
- * (each launch resets what must start at zero). Calls that overlap on the GPU,
+ * (each call resets its barrier words first). Calls that overlap on the GPU,
  * such as calls on two streams with no ordering between them, race on it.
  */
 int ep_get_dispatch_layout_noalloc(const ep_layout_t* L, int32_t* status, void* stream);
@@ -339,10 +345,13 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *   recv_x       [E, R*T, hidden] BF16, or E4M3 with EP_FP8
  *   recv_scales  [E, R*T, hidden/128] fp32, or UE8M0 bytes (FP8 only)
  *   recv_src     [E, R*T] int32: global token index of each written row
- *   workspace    at least ep_ll_workspace_bytes(...) bytes; afterwards it
+ *   workspace    at least ep_ll_workspace_bytes(...) bytes, zero-filled
+ *                before its first use (as for ep_get_dispatch_layout: each
+ *                send leaves its barrier words zero again); afterwards it
  *                holds the routing that receive and combine use, until the
  *                next send on it
- *   status       EP_ST_BAD_INDEX as for the layout
+ *   status       EP_ST_BAD_INDEX, EP_ST_TIMEOUT and EP_ST_WORKSPACE as for
+ *                the layout
  * Enqueues two launches. The rows are in place when the stream reaches the
  * end of this call; the counts are published by ep_ll_dispatch_recv.
  */

@@ -42,6 +42,7 @@ def test_version_and_error_strings(L):
     assert L.ep_version() >= 100
     assert ep.ep_error_string(ep.EP_ERR_LL_CAPACITY).startswith("low-latency")
     assert ep.ep_error_string(ep.EP_ST_NOT_SENT).startswith("status")
+    assert "zero-fill" in ep.ep_error_string(ep.EP_ST_WORKSPACE)
     assert ep.ep_error_string(0) == "ok"
 
 

@@ -100,7 +100,7 @@ def test_normal_path_in_a_cuda_graph():
     idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
     w = torch.empty((N, K), dtype=torch.float32, device="cuda")
     lay = ep.new_layout(idx, E, R)
-    ws = torch.empty(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device="cuda")
     ex = torch.empty((N * K, H), dtype=torch.uint8, device="cuda")
     es = torch.empty((N * K, H // 128), dtype=torch.float32, device="cuda")
     ysrc = torch.empty((N * K, H), dtype=torch.bfloat16, device="cuda")

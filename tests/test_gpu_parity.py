@@ -110,6 +110,34 @@ def test_layout_deterministic_repeat():
         assert torch.equal(getattr(a, k), getattr(b, k))
 
 
+def test_layout_workspace_left_clean_and_dirty_one_flagged():
+    """The grid barrier clears its own words: calls on one zero-filled workspace
+    stay exact with no reset in between; barrier words found non-zero (a
+    workspace never zero-filled) are reported with EP_ST_WORKSPACE."""
+    cfg = ei.CONFIGS[4].scaled(N=2048)          # 12288 entries: a dozen CTAs, so a real grid barrier
+    idx, _ = ei.make_routing(cfg, 50)
+    ref = oracle.layout(idx, cfg.E, cfg.R)
+    ws = torch.zeros(ep.ep_layout_workspace_bytes(cfg.N, cfg.K, cfg.E, cfg.R), dtype=torch.uint8, device="cuda")
+    lay = ep.new_layout(to_dev(idx), cfg.E, cfg.R)
+    for _ in range(3):
+        st = _status()
+        ep.ep_get_dispatch_layout(lay, ws, st)
+        _layout_equal(lay, ref)
+        assert status_value(st) == 0
+        assert int(ws[:8].sum().item()) == 0    # both barrier words are zero again
+    # Leftover bytes: 0x01010101 is far above the block count, so every block
+    # passes the barrier at once and the one check that matters fires.
+    ws[:8] = 1
+    st = _status()
+    ep.ep_get_dispatch_layout(lay, ws, st)
+    assert status_value(st) & ep.EP_ST_WORKSPACE
+    ws[:8] = 0
+    st = _status()
+    ep.ep_get_dispatch_layout(lay, ws, st)
+    _layout_equal(lay, ref)
+    assert status_value(st) == 0
+
+
 # ---------------------------------------------------------------- dispatch ----
 def _check_dispatch(res, ref, use_fp8, K, with_rank=True):
     conv = u8 if use_fp8 else u16
