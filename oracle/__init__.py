@@ -66,6 +66,10 @@ def lib():
         L.oracle_gather_rows.restype = i32
         L.oracle_combine_staged.argtypes = [P, P, P, i32, i32, i32, P]
         L.oracle_combine_staged.restype = i32
+        L.oracle_ll_mask_routing.argtypes = [P, i32, i32, i32, i32, P, P]
+        L.oracle_ll_mask_routing.restype = i32
+        L.oracle_ll_mask_slot_map.argtypes = [P, i32, i32, i32, i32, i32, P, P]
+        L.oracle_ll_mask_slot_map.restype = i32
         _lib = L
     return _lib
 
@@ -224,11 +228,40 @@ def combine_to_ranks(y_bf16: np.ndarray, topk_idx: np.ndarray, lay: dict, topk_w
     return out, int(st)
 
 
+def ll_mask_routing(topk_idx: np.ndarray, E: int, R: int, rank_mask: np.ndarray) -> np.ndarray:
+    """Shrink mode: the routing with every slot of a masked rank (the expert's
+    rank, or the token's source rank) set to -1."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    m = np.ascontiguousarray(rank_mask, dtype=np.int32)
+    assert m.shape == (R,)
+    N, K = idx.shape
+    out = np.empty_like(idx)
+    lib().oracle_ll_mask_routing(_p(idx), N, K, E, R, _p(m), _p(out))
+    return out
+
+
+def ll_mask_slot_map(slot_map: np.ndarray, E: int, R: int, T: int, rank_mask: np.ndarray) -> np.ndarray:
+    """Shrink mode at combine time: slot-map entries of masked ranks set to -1."""
+    slot = np.ascontiguousarray(slot_map, dtype=np.int32)
+    m = np.ascontiguousarray(rank_mask, dtype=np.int32)
+    assert m.shape == (R,)
+    N, K = slot.shape
+    out = np.empty_like(slot)
+    lib().oracle_ll_mask_slot_map(_p(slot), N, K, E, R, T, _p(m), _p(out))
+    return out
+
+
 def ll_dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, E: int, R: int, T: int,
-                use_fp8: bool, round_scale: bool = False, ue8m0: bool = False) -> dict:
-    """Low-latency dispatch into the fixed [E, R*T, H] buffer (global view)."""
+                use_fp8: bool, round_scale: bool = False, ue8m0: bool = False,
+                rank_mask: Optional[np.ndarray] = None) -> dict:
+    """Low-latency dispatch into the fixed [E, R*T, H] buffer (global view).
+
+    rank_mask [R] (shrink mode): slots of masked ranks are dropped first.
+    """
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    if rank_mask is not None:
+        idx = ll_mask_routing(idx, E, R, rank_mask)
     N, H = x.shape
     K = idx.shape[1]
     xdt = np.uint8 if use_fp8 else np.uint16
@@ -248,8 +281,15 @@ def ll_dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, E: int, R: int, T: int
     return o
 
 
-def ll_combine(y_bf16: np.ndarray, slot_map: np.ndarray, topk_weights: np.ndarray) -> tuple:
-    """Low-latency combine: y is [E, R*T, H]; slot_map rows index its flattened view."""
+def ll_combine(y_bf16: np.ndarray, slot_map: np.ndarray, topk_weights: np.ndarray,
+               rank_mask: Optional[np.ndarray] = None, R: Optional[int] = None) -> tuple:
+    """Low-latency combine: y is [E, R*T, H]; slot_map rows index its flattened view.
+
+    rank_mask [R] (shrink mode, R given): slots of ranks masked now are skipped.
+    """
+    if rank_mask is not None:
+        E, RT = y_bf16.shape[0], y_bf16.shape[1]
+        slot_map = ll_mask_slot_map(slot_map, E, R, RT // R, rank_mask)
     return combine(y_bf16.reshape(-1, y_bf16.shape[-1]), slot_map, topk_weights)
 
 

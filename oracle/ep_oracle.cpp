@@ -488,4 +488,47 @@ int oracle_ll_dispatch(const uint16_t* x, const int32_t* idx, int N, int K, int 
   return status;
 }
 
+// Shrink mode ("DeepEP V1 (legacy) guide", section 6.4: a rank can be masked
+// out online with low_latency_update_mask_buffer and restored with
+// low_latency_clean_mask_buffer). A masked rank neither sends nor receives,
+// so a (token, slot) is dropped, exactly as if its index were -1, when the
+// rank holding its expert (e / L) or the token's source rank (t / n_s, n_s =
+// N / R) is masked. Out-of-range indices are left as they are (the dispatch
+// reports them).
+int oracle_ll_mask_routing(const int32_t* idx, int N, int K, int E, int R, const int32_t* rank_mask,
+                           int32_t* out) {
+  const int L = E / R;
+  const int n_s = N / R;
+  for (int t = 0; t < N; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int64_t tk = static_cast<int64_t>(t) * K + k;
+      const int32_t e = idx[tk];
+      out[tk] = e;
+      if (!valid_expert(e, E)) continue;
+      const int src = n_s > 0 ? t / n_s : 0;
+      if (rank_mask[e / L] != 0 || (src < R && rank_mask[src] != 0)) out[tk] = -1;
+    }
+  return 0;
+}
+
+// The same rule applied when the combine runs to a low-latency slot map
+// (entries e * R*T + j, or -1): the mask may have changed since the send.
+int oracle_ll_mask_slot_map(const int32_t* slot_map, int N, int K, int E, int R, int T,
+                            const int32_t* rank_mask, int32_t* out) {
+  const int L = E / R;
+  const int n_s = N / R;
+  const int64_t cap = static_cast<int64_t>(R) * T;
+  for (int t = 0; t < N; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int64_t tk = static_cast<int64_t>(t) * K + k;
+      const int32_t row = slot_map[tk];
+      out[tk] = row;
+      if (row < 0) continue;
+      const int e = static_cast<int>(row / cap);
+      const int src = n_s > 0 ? t / n_s : 0;
+      if (rank_mask[e / L] != 0 || (src < R && rank_mask[src] != 0)) out[tk] = -1;
+    }
+  return 0;
+}
+
 }  // extern "C"

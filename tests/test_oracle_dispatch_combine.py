@@ -260,6 +260,66 @@ def test_two_phase_ll_combine_equals_single_phase():
     assert np.array_equal(two, one)
 
 
+def test_shrink_mask_hand_example():
+    # "DeepEP V1 (legacy) guide" 6.4 (shrink mode): a masked rank neither sends
+    # nor receives, so its experts' slots and its own tokens' slots drop out.
+    # 4 tokens, 2 ranks of 2 experts, tokens 0-1 from rank 0 and 2-3 from rank 1.
+    N, K, E, R, T, H = 4, 2, 4, 2, 2, 8
+    idx = np.array([[0, 2], [3, 1], [2, -1], [1, 3]], np.int32)
+    x = ei.bf16_bits_from_f32(np.arange(N * H, dtype=np.float32).reshape(N, H) + 1)
+    # rank 1 masked at the send: only (t0 -> e0) and (t1 -> e1) remain
+    ll = oracle.ll_dispatch(x, idx, E, R, T, False, rank_mask=np.array([0, 1], np.int32))
+    assert ll["status"] == 0
+    assert ll["recv_count"].tolist() == [1, 1, 0, 0]
+    assert ll["slot_map"].tolist() == [[0, -1], [-1, 4], [-1, -1], [-1, -1]]
+    assert np.array_equal(ll["recv_x"][0, 0], x[0]) and np.array_equal(ll["recv_x"][1, 0], x[1])
+    assert ll["recv_src"][0].tolist() == [0, -1, -1, -1] and ll["recv_src"][1].tolist() == [1, -1, -1, -1]
+    assert ll["layout_range"].tolist() == [[1, 1 << 32], [1, 1 << 32], [0, 0], [0, 0]]
+    # nothing masked at the send; rank 0 is lost before the combine
+    full = oracle.ll_dispatch(x, idx, E, R, T, False)
+    assert full["slot_map"].tolist() == [[0, 8], [12, 4], [9, -1], [5, 13]]
+    y = np.repeat(np.arange(1, E * R * T + 1, dtype=np.float32)[:, None], H, axis=1)   # row r holds r + 1
+    y = ei.bf16_bits_from_f32(y).reshape(E, R * T, H)
+    w = np.array([[1, 1], [1, 1], [0.5, 1], [1, 0.25]], np.float32)
+    out, st = oracle.ll_combine(y, full["slot_map"], w, rank_mask=np.array([1, 0], np.int32), R=R)
+    of = oracle.f32_from_bf16(out)
+    assert st == 0
+    assert out[0].tolist() == [0] * H and out[1].tolist() == [0] * H   # rank 0's tokens: +0
+    assert np.all(of[2] == 0.5 * 10) and np.all(of[3] == 0.25 * 14)    # only rank 1's experts count
+
+
+def test_shrink_mask_degenerate_cases():
+    cfg = ei.CONFIGS[2].scaled(N=32 * 8, H=256)
+    x, idx, w = _inputs(cfg, seed=6)
+    R, E, T = cfg.R, cfg.E, cfg.T
+    plain = oracle.ll_dispatch(x, idx, E, R, T, True)
+    none = oracle.ll_dispatch(x, idx, E, R, T, True, rank_mask=np.zeros(R, np.int32))
+    for k in ("recv_x", "recv_scales", "recv_src", "recv_count", "layout_range", "slot_map"):
+        assert np.array_equal(plain[k], none[k]), k
+    every = oracle.ll_dispatch(x, idx, E, R, T, True, rank_mask=np.ones(R, np.int32))
+    assert every["recv_count"].sum() == 0 and np.all(every["slot_map"] == -1)
+    # masking ranks = the unmasked dispatch of the routing with their slots set to -1
+    m = np.zeros(R, np.int32)
+    m[[3, 17]] = 1
+    L, n_s = E // R, cfg.N // R
+    idx_m = idx.copy()
+    for t in range(cfg.N):
+        for k in range(cfg.K):
+            if idx[t, k] >= 0 and (m[idx[t, k] // L] or m[t // n_s]):
+                idx_m[t, k] = -1
+    a = oracle.ll_dispatch(x, idx, E, R, T, True, rank_mask=m)
+    b = oracle.ll_dispatch(x, idx_m, E, R, T, True)
+    for k in ("recv_x", "recv_scales", "recv_src", "recv_count", "layout_range", "slot_map"):
+        assert np.array_equal(a[k], b[k]), k
+    y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(9, 4), plain["recv_x"].size).astype(np.float32))
+    y = y.reshape(plain["recv_x"].shape)
+    out, _ = oracle.ll_combine(y, plain["slot_map"], w, rank_mask=np.ones(R, np.int32), R=R)
+    assert np.all(out == 0)
+    same, _ = oracle.ll_combine(y, plain["slot_map"], w, rank_mask=np.zeros(R, np.int32), R=R)
+    ref, _ = oracle.ll_combine(y, plain["slot_map"], w)
+    assert np.array_equal(same, ref)
+
+
 def test_bias_is_added_after_the_weighted_sum():
     # "DeepEP Ascend deep dive", "Combine: More Output, Same Cost": the shared
     # expert's output is added as a bias in the epilogue. Hand-derived: terms
