@@ -68,6 +68,8 @@ def parse():
                     help="normal workloads: also the backward passes (combine backward, then dispatch backward)")
     ap.add_argument("--ll-combine", default="one-phase", choices=["one-phase", "two-phase"],
                     help="low-latency workloads: combine in one launch, or send + receive hook")
+    ap.add_argument("--mask-ranks", default="",
+                    help="low-latency workloads: comma-separated ranks masked in the workspace (shrink mode)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
@@ -426,6 +428,8 @@ def run_ours(args):
     if cfg.mode == "ll":
         wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase", scales=args.fp8_scales,
                         bias=args.combine_bias)
+        for r in (int(v) for v in args.mask_ranks.split(",") if v):
+            ep.low_latency_update_mask_buffer(wl.ws, r, num_ranks=cfg.R)   # shrink mode: rank r is out
     else:
         wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales, align=args.expert_alignment,
                             bias=args.combine_bias, two_level=args.combine == "two-level", training=args.training)
@@ -563,7 +567,8 @@ def run_ours(args):
                    "l2": "flushed between steps (256 MiB write)",
                    "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
                                "combine": args.combine, "ll_combine": args.ll_combine,
-                               "fp8_scales": args.fp8_scales, "training": args.training},
+                               "fp8_scales": args.fp8_scales, "training": args.training,
+                               "mask_ranks": args.mask_ranks},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "rows": wl.rows()},
         "phases": phases,

@@ -123,6 +123,9 @@ def lib() -> ctypes.CDLL:
         "ep_fp8_e4m3_encode": (I, [P, P, I64, P]),
         "ep_ll_combine_send": (I, [P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_ll_combine_recv": (I, [P, P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
+        "ep_ll_update_mask": (I, [P, SZ, I, I, I, P]),
+        "ep_ll_query_mask": (I, [P, SZ, I, P, P]),
+        "ep_ll_clean_mask": (I, [P, SZ, I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -302,6 +305,23 @@ def ep_ll_combine_recv(staging, topk_weights, workspace, N, K, H, E, R, T, out, 
                        stream=None, bias=None) -> None:
     _check(lib().ep_ll_combine_recv(_p(staging), _p(topk_weights), _p(bias), _p(workspace), workspace.numel(), N,
                                     K, H, E, R, T, _p(out), _p(status), _stream(stream)), "ep_ll_combine_recv")
+
+
+def ep_ll_update_mask(workspace, R, rank, masked=True, stream=None) -> None:
+    _check(lib().ep_ll_update_mask(_p(workspace), workspace.numel(), R, rank, int(bool(masked)),
+                                   _stream(stream)), "ep_ll_update_mask")
+
+
+def ep_ll_query_mask(workspace, R, out=None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(R, dtype=torch.int32, device=workspace.device)
+    _check(lib().ep_ll_query_mask(_p(workspace), workspace.numel(), R, _p(out), _stream(stream)),
+           "ep_ll_query_mask")
+    return out
+
+
+def ep_ll_clean_mask(workspace, R, stream=None) -> None:
+    _check(lib().ep_ll_clean_mask(_p(workspace), workspace.numel(), R, _stream(stream)), "ep_ll_clean_mask")
 
 
 def ep_fp8_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
@@ -529,3 +549,35 @@ def low_latency_combine(expert_y: torch.Tensor, topk_weights: torch.Tensor, hand
         ep_ll_combine_recv(staging, w, h.workspace, h.N, h.K, h.H, h.E, h.R, h.T, out, status, stream, bias=b)
 
     return out, hook
+
+
+# ------------------------------------------------- shrink mode (rank masks) ----
+def _ws_ranks(handle, num_ranks):
+    if isinstance(handle, LLHandle):
+        return handle.workspace, handle.R
+    if num_ranks is None:
+        raise ValueError("num_ranks is needed with a bare workspace tensor")
+    return handle, num_ranks
+
+
+def low_latency_update_mask_buffer(handle, rank: int, mask: bool = True, num_ranks: Optional[int] = None,
+                                   stream=None) -> None:
+    """Shrink mode ("DeepEP V1 (legacy) guide", section 6.4): mask (or, with
+    mask=False, restore) rank `rank` in the low-latency workspace. handle is
+    an LLHandle or the workspace tensor itself (then num_ranks is needed).
+    Sends on that workspace drop every slot whose expert lives on a masked
+    rank or whose token comes from one; combines skip them as well."""
+    ws, R = _ws_ranks(handle, num_ranks)
+    ep_ll_update_mask(ws, R, rank, mask, stream)
+
+
+def low_latency_query_mask_buffer(handle, num_ranks: Optional[int] = None, stream=None) -> torch.Tensor:
+    """The current rank mask, [R] int32 on the device (non-zero = masked)."""
+    ws, R = _ws_ranks(handle, num_ranks)
+    return ep_ll_query_mask(ws, R, stream=stream)
+
+
+def low_latency_clean_mask_buffer(handle, num_ranks: Optional[int] = None, stream=None) -> None:
+    """Restore every rank."""
+    ws, R = _ws_ranks(handle, num_ranks)
+    ep_ll_clean_mask(ws, R, stream)

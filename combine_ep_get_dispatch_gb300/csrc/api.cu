@@ -56,14 +56,17 @@ LayoutWs layout_ws(int N, int K, int E, int R) {
   return w;
 }
 
-// Low-latency workspace: header, counts, ranges, slot map, chunk counts, barrier.
+// Low-latency workspace: header, shrink-mode rank mask (at a fixed offset, so
+// the mask calls need only R), counts, ranges, slot map, chunk counts, barrier.
+constexpr size_t kLLMaskOffset = 256;
 struct LLWs {
-  size_t hdr, count, range, slot, chunk, barrier, total;
+  size_t hdr, mask, count, range, slot, chunk, barrier, total;
 };
 LLWs ll_ws(int N, int K, int E, int R) {
   LLWs w;
   w.hdr = 0;
-  w.count = 256;
+  w.mask = kLLMaskOffset;
+  w.count = w.mask + align256(sizeof(int32_t) * R);
   w.range = w.count + align256(sizeof(int32_t) * E);
   w.slot = w.range + align256(sizeof(int64_t) * static_cast<size_t>(E) * R);
   w.chunk = w.slot + align256(sizeof(int32_t) * static_cast<size_t>(N) * K);
@@ -300,6 +303,14 @@ size_t ep_ll_workspace_bytes(int N, int K, int E, int R, int T) {
   return ll_ws(N, K, E, R).total;
 }
 
+// The combine side of shrink mode: the mask as it stands when the combine runs.
+static void set_ll_mask(CombineParams& p, void* ws, const LLWs& w, int N, int E, int R, int T) {
+  p.rank_mask = at<int32_t>(ws, w.mask);
+  p.ll_cap = static_cast<int64_t>(R) * T;
+  p.ll_L = E / R;
+  p.ll_ns = N / R > 0 ? N / R : 1;
+}
+
 static int ll_common_checks(int N, int K, int E, int R, int T) {
   if (!sizes_ok(N, K, E, R) || T < 1) return EP_ERR_INVALID_ARG;
   if (N % R != 0) return EP_ERR_INVALID_ARG;
@@ -336,6 +347,7 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   lp.hdr_value = LLHeader{kMagicSent, N, K, E, R, T, H, use_fp8, 0};
   lp.ws_chunk = at<int32_t>(workspace, w.chunk);
   lp.ws_barrier = at<unsigned>(workspace, w.barrier);
+  lp.rank_mask = at<int32_t>(workspace, w.mask);
   lp.status = status;
   rc = cuda_rc(launch_layout(lp, R, false, true, s));
   if (rc != EP_OK) return rc;
@@ -398,6 +410,7 @@ int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* b
   p.N = N; p.K = K; p.H = H;
   p.ll_hdr = at<LLHeader>(ws, w.hdr);
   p.ll_expect = LLHeader{kMagicSent, N, K, E, R, T, H, 0, 0};
+  set_ll_mask(p, ws, w, N, E, R, T);
   p.status = status;
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
@@ -421,6 +434,7 @@ int ep_ll_combine_send(const void* expert_y, const void* workspace, size_t works
   p.gather = 1;
   p.ll_hdr = at<LLHeader>(ws, w.hdr);
   p.ll_expect = LLHeader{kMagicSent, N, K, E, R, T, H, 0, 0};
+  set_ll_mask(p, ws, w, N, E, R, T);
   p.status = status;
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
 }
@@ -447,8 +461,33 @@ int ep_ll_combine_recv(const void* staging, const float* topk_weights, const voi
   p.N = N; p.K = K; p.H = H;
   p.ll_hdr = at<LLHeader>(ws, w.hdr);
   p.ll_expect = LLHeader{kMagicSent, N, K, E, R, T, H, 0, 0};
+  set_ll_mask(p, ws, w, N, E, R, T);
   p.status = status;
   return cuda_rc(launch_combine(p, static_cast<cudaStream_t>(stream)));
+}
+
+static int ll_mask_call(void* workspace, size_t workspace_bytes, int R, int mode, int rank, int value,
+                        int32_t* out, void* stream) {
+  if (R < 1 || R > EP_MAX_EXPERTS) return EP_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < kLLMaskOffset + sizeof(int32_t) * R) return EP_ERR_WORKSPACE;
+  return cuda_rc(launch_ll_mask(at<int32_t>(workspace, kLLMaskOffset), R, mode, rank, value, out,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int ep_ll_update_mask(void* workspace, size_t workspace_bytes, int num_ranks, int rank, int masked,
+                      void* stream) {
+  if (rank < 0 || rank >= num_ranks) return EP_ERR_INVALID_ARG;
+  return ll_mask_call(workspace, workspace_bytes, num_ranks, 0, rank, masked ? 1 : 0, nullptr, stream);
+}
+
+int ep_ll_query_mask(const void* workspace, size_t workspace_bytes, int num_ranks, int32_t* mask_out,
+                     void* stream) {
+  if (!mask_out) return EP_ERR_INVALID_ARG;
+  return ll_mask_call(const_cast<void*>(workspace), workspace_bytes, num_ranks, 1, 0, 0, mask_out, stream);
+}
+
+int ep_ll_clean_mask(void* workspace, size_t workspace_bytes, int num_ranks, void* stream) {
+  return ll_mask_call(workspace, workspace_bytes, num_ranks, 2, 0, 0, nullptr, stream);
 }
 
 int ep_fp8_e4m3_encode(const float* in, uint8_t* out, int64_t n, void* stream) {

@@ -77,6 +77,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int v1 = min(nvec, v0 + span);
     for (int k = tid; k < K; k += kThreads) {
       int32_t row = __ldg(p.slot + t * K + k);
+      // Low-latency shrink mode: skip the slots of ranks masked now (the
+      // expert's rank, from its region e = row / (R*T), or the token's source).
+      if (row >= 0 && p.rank_mask &&
+          (__ldg(p.rank_mask + static_cast<int>(row / p.ll_cap) / p.ll_L) != 0 ||
+           __ldg(p.rank_mask + static_cast<int>(t / p.ll_ns)) != 0))
+        row = -1;
       if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + k);
       if (row >= p.y_rows) {
         flag(p.status, EP_ST_CAPACITY);

@@ -35,6 +35,7 @@ struct LayoutParams {
   int64_t* ll_range;   // [E, R]
   LLHeader* ll_hdr;
   LLHeader hdr_value;
+  const int32_t* rank_mask;  // low-latency shrink mode: [R], non-zero = masked (or null)
   // scratch
   int32_t* ws_chunk;   // [G, C]
   unsigned* ws_barrier;
@@ -78,6 +79,10 @@ struct CombineParams {
   int gather;            // copy every routed row to out[t*K + k] instead of summing
   const LLHeader* ll_hdr;  // low-latency: the send's header (null in normal mode)
   LLHeader ll_expect;
+  // low-latency shrink mode: slots of masked ranks are skipped (rank_mask null: none)
+  const int32_t* rank_mask;  // [R]
+  int64_t ll_cap;            // R * T rows per expert region
+  int ll_L, ll_ns;           // experts per rank, tokens per source rank
   int32_t* status;
 };
 
@@ -140,6 +145,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s);
 cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s);
 cudaError_t launch_pad_zero(const PadParams& p, cudaStream_t s);
+cudaError_t launch_ll_mask(int32_t* mask, int R, int mode, int rank, int value, int32_t* out, cudaStream_t s);
 cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
 

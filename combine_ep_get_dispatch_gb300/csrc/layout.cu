@@ -117,6 +117,14 @@ __device__ __forceinline__ int entry_code_global(const LayoutParams& p, int64_t 
   return code;
 }
 
+// Low-latency shrink mode: an entry is dropped (as if its index were -1) when
+// its source rank (the CTA's chunk) or the rank holding its expert is masked.
+template <bool kLL>
+__device__ __forceinline__ bool ll_drop(const LayoutParams& p, int code, bool src_masked) {
+  if (!kLL || code < 0 || !p.rank_mask) return false;
+  return src_masked || __ldg(p.rank_mask + code_r(code)) != 0;
+}
+
 template <bool kRank, bool kLL, bool kStaged>
 __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutParams p) {
   extern __shared__ int32_t sm[];
@@ -144,6 +152,9 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   int32_t* scode = part + 2 * PS;      // [tokens_per_cta * K]: entry codes (kStaged)
 
   bool bad = false;
+  // Low-latency shrink mode: a masked source rank sends nothing (this CTA's
+  // chunk is that rank's tokens).
+  const bool src_masked = kLL && p.rank_mask && __ldg(p.rank_mask + cta) != 0;
   for (int i = tid; i < W * CP; i += NT) hist[i] = 0;
   if (kRank) {
     for (int64_t i = t0 * R + tid; i < t1 * R; i += NT) {
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
         else
           bad = true;
       }
-      scode[li] = code;
+      scode[li] = ll_drop<kLL>(p, code, src_masked) ? -1 : code;
     }
     __syncthreads();
     if (kRank) {
@@ -188,7 +199,8 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
 
   // Pass 1: per-warp counts (shared-memory atomics: counting needs no order).
   for (int li = wa0 + lane; li < wa1; li += 32) {
-    const int code = kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad);
+    int code = kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad);
+    if (!kStaged && ll_drop<kLL>(p, code, src_masked)) code = -1;
     if (code >= 0) {
       atomicAdd(&my[code_e(code)], 1);
       if (kRank && (code & kFirstBit)) atomicAdd(&my[E + code_r(code)], 1);
@@ -287,7 +299,8 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   for (int b = wa0; b < wa1; b += 32) {
     const int li = b + lane;
     const bool in = li < wa1;
-    const int code = in ? (kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad2)) : -1;
+    int code = in ? (kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad2)) : -1;
+    if (!kStaged && ll_drop<kLL>(p, code, src_masked)) code = -1;
     const bool valid = code >= 0;
     const int e = code_e(code);
     const unsigned pe = warp_peers(e, valid, p.bits_E);

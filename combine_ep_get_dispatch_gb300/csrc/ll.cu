@@ -58,6 +58,16 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParam
   if (tid == 0) p.hdr->magic = kMagicReceived;
 }
 
+// Shrink-mode mask buffer: mode 0 sets mask[rank] = value, 1 copies the mask
+// to out, 2 clears it.
+__global__ void ll_mask_kernel(int32_t* mask, int R, int mode, int rank, int value, int32_t* out) {
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    if (mode == 0 && i == rank) mask[i] = value;
+    if (mode == 1) out[i] = mask[i];
+    if (mode == 2) mask[i] = 0;
+  }
+}
+
 __global__ void e4m3_encode_kernel(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
@@ -68,6 +78,11 @@ __global__ void e4m3_encode_kernel(const float* __restrict__ in, uint8_t* __rest
 
 cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s) {
   ll_recv_kernel<<<1, kRecvThreads, 0, s>>>(p, E, R);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ll_mask(int32_t* mask, int R, int mode, int rank, int value, int32_t* out, cudaStream_t s) {
+  ll_mask_kernel<<<1, 256, 0, s>>>(mask, R, mode, rank, value, out);
   return cudaGetLastError();
 }
 

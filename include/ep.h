@@ -352,7 +352,8 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *                next send on it
  *   status       EP_ST_BAD_INDEX, EP_ST_TIMEOUT and EP_ST_WORKSPACE as for
  *                the layout
- * Enqueues two launches. The rows are in place when the stream reaches the
+ * Slots of ranks masked in the workspace (shrink mode, ep_ll_update_mask)
+ * are dropped. Enqueues two launches. The rows are in place when the stream reaches the
  * end of this call; the counts are published by ep_ll_dispatch_recv.
  */
 int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, int num_topk,
@@ -397,6 +398,7 @@ int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int num_tokens,
  *   workspace     filled by the send of this batch (same sizes)
  *   out           [N, hidden] BF16
  *   status        EP_ST_NOT_SENT / EP_ST_MISMATCH as for the receive
+ * Slots of ranks masked in the workspace now (shrink mode) are skipped.
  */
 int ep_ll_combine(const void* expert_y, const float* topk_weights, const void* bias,
                   const void* workspace, size_t workspace_bytes, int num_tokens, int num_topk,
@@ -439,6 +441,34 @@ int ep_ll_combine_recv(const void* staging, const float* topk_weights, const voi
                        const void* workspace, size_t workspace_bytes, int num_tokens, int num_topk,
                        int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
                        void* out, int32_t* status, void* stream);
+
+/*
+ * Shrink mode: masking ranks of the low-latency path online ("DeepEP V1
+ * (legacy) guide", section 6.4: low_latency_update_mask_buffer /
+ * low_latency_query_mask_buffer / low_latency_clean_mask_buffer, used for
+ * fault tolerance when a rank is lost).
+ *
+ * The low-latency workspace holds one int32 per rank, 0 (active) in a
+ * zero-filled workspace, and it persists across sends. A masked rank neither
+ * sends nor receives: a (token, slot) is dropped, exactly as if its index
+ * were -1, when the rank holding its expert (e / (E/R)) or the token's source
+ * rank (t / (N/R)) is masked. ep_ll_dispatch_send applies the mask as it
+ * stands when the send runs (dropped slots are not written, counted or put in
+ * the ranges); ep_ll_combine and both combine phases apply it as it stands
+ * when they run, so a rank lost between send and combine is skipped there
+ * too (a token of a masked source rank combines to +0).
+ *
+ *   workspace  a low-latency workspace (at least 256 + 4 * num_ranks bytes;
+ *              normally the ep_ll_workspace_bytes(...) one the sends use)
+ *   rank       0 <= rank < num_ranks; masked != 0 masks it, 0 restores it
+ *   mask_out   [num_ranks] int32 device buffer: the current mask
+ * Each call is one small launch on the stream, ordered like the others.
+ */
+int ep_ll_update_mask(void* workspace, size_t workspace_bytes, int num_ranks, int rank, int masked,
+                      void* stream);
+int ep_ll_query_mask(const void* workspace, size_t workspace_bytes, int num_ranks, int32_t* mask_out,
+                     void* stream);
+int ep_ll_clean_mask(void* workspace, size_t workspace_bytes, int num_ranks, void* stream);
 
 /*
  * Element-wise fp32 -> FP8 E4M3 conversion (round to nearest even, saturated

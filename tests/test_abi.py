@@ -102,6 +102,12 @@ def test_host_validation_rejects_before_cuda(L):
     assert L.ep_ll_combine(P(16), P(16), None, P(256), 1 << 30, 128, 8, 100, 256, 8, 128, P(16), None, None) \
         == ep.EP_ERR_INVALID_ARG  # hidden % 8 != 0
     assert L.ep_fp8_e4m3_encode(None, None, -1, None) == ep.EP_ERR_INVALID_ARG
+    # shrink-mode mask calls: rank range, rank count, workspace size
+    assert L.ep_ll_update_mask(P(256), 1 << 20, 8, 8, 1, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_ll_update_mask(P(256), 1 << 20, 0, 0, 1, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_ll_update_mask(P(256), 64, 8, 0, 1, None) == ep.EP_ERR_WORKSPACE
+    assert L.ep_ll_query_mask(P(256), 1 << 20, 8, None, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_ll_clean_mask(None, 0, 8, None) == ep.EP_ERR_WORKSPACE
 
 
 def test_package_has_no_cpu_fallback():

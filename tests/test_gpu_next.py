@@ -30,7 +30,9 @@ def _expert_outputs(shape, seed):
 
 @pytest.mark.parametrize("c,n_s,H", [(1, 16, 7168), (2, 16, 1024)])
 def test_two_phase_ll_combine(c, n_s, H):
-    cfg = ei.CONFIGS[c].scaled(N=ei.CONFIGS[c].R * n_s, H=H)
+    # T = 32 only sizes the fixed regions (rows are packed from 0), and keeps
+    # the host copy of the [E, R*T, H] expert outputs small.
+    cfg = ei.CONFIGS[c].scaled(N=ei.CONFIGS[c].R * n_s, H=H, T=32)
     d = ei.make_inputs(cfg, seed=c + 20)
     st = _status()
     recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), cfg.T, cfg.E,
@@ -290,4 +292,70 @@ def test_dispatch_and_combine_backward():
     # deterministic: the same bits on a second run
     gy2, gw2 = ep.combine_backward(to_dev_bf16(g), lay, to_dev_bf16(y), to_dev(w), status=st)
     assert torch.equal(gy, gy2) and np.array_equal(gw, gw2.cpu().numpy().astype(np.float64))
+    assert status_value(st) == 0
+
+
+# ------------------------------------------------- shrink mode (rank masks) ----
+def test_shrink_mask_buffer_update_query_clean():
+    R = 8
+    ws = torch.zeros(ep.ep_ll_workspace_bytes(64, 8, 64, R, 16), dtype=torch.uint8, device="cuda")
+    assert ep.low_latency_query_mask_buffer(ws, num_ranks=R).tolist() == [0] * R
+    ep.low_latency_update_mask_buffer(ws, 3, num_ranks=R)
+    ep.low_latency_update_mask_buffer(ws, 5, num_ranks=R)
+    assert ep.low_latency_query_mask_buffer(ws, num_ranks=R).tolist() == [0, 0, 0, 1, 0, 1, 0, 0]
+    ep.low_latency_update_mask_buffer(ws, 3, mask=False, num_ranks=R)
+    assert ep.low_latency_query_mask_buffer(ws, num_ranks=R).tolist() == [0, 0, 0, 0, 0, 1, 0, 0]
+    ep.low_latency_clean_mask_buffer(ws, num_ranks=R)
+    assert ep.low_latency_query_mask_buffer(ws, num_ranks=R).tolist() == [0] * R
+    with pytest.raises(ep.EPError):
+        ep.low_latency_update_mask_buffer(ws, R, num_ranks=R)
+
+
+@pytest.mark.parametrize("c,n_s,H,T", [(1, 16, 2048, 32), (2, 16, 512, 16)])
+def test_shrink_send_and_combine(c, n_s, H, T):
+    """Ranks masked before the send drop out of the receive buffers; a rank lost
+    between send and combine is skipped by the one- and the two-phase combine."""
+    cfg = ei.CONFIGS[c].scaled(N=ei.CONFIGS[c].R * n_s, H=H, T=T)
+    N, K, E, R, T = cfg.N, cfg.K, cfg.E, cfg.R, cfg.T
+    d = ei.make_inputs(cfg, seed=c + 70)
+    st = _status()
+    ws = torch.zeros(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device="cuda")
+    m_send = np.zeros(R, np.int32)
+    m_send[[1, R - 2]] = 1
+    for r in np.nonzero(m_send)[0]:
+        ep.low_latency_update_mask_buffer(ws, int(r), num_ranks=R)
+    recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), T, E, R,
+                                                      use_fp8=cfg.fp8, status=st, workspace=ws)
+    hook()
+    ref = oracle.ll_dispatch(d["x"], d["topk_idx"], E, R, T, cfg.fp8, rank_mask=m_send)
+    cnt = cnt.cpu().numpy()
+    assert np.array_equal(cnt, ref["recv_count"])
+    assert cnt.sum() < np.count_nonzero(d["topk_idx"] >= 0)          # something was dropped
+    assert np.array_equal(handle.layout_range.cpu().numpy(), ref["layout_range"])
+    rx, rs = recv if cfg.fp8 else (recv, None)
+    gx = u8(rx) if cfg.fp8 else u16(rx)
+    src = handle.recv_src.cpu().numpy()
+    for e in range(E):
+        n = cnt[e]
+        assert np.array_equal(gx[e, :n], ref["recv_x"][e, :n])
+        assert np.array_equal(src[e, :n], ref["recv_src"][e, :n])
+        if cfg.fp8:
+            assert np.array_equal(rs[e, :n].cpu().numpy(), ref["recv_scales"][e, :n])
+    # the mask changes before the combine: rank 2 is lost, rank R-2 is back
+    m_comb = m_send.copy()
+    m_comb[2], m_comb[R - 2] = 1, 0
+    ep.low_latency_update_mask_buffer(handle, 2)
+    ep.low_latency_update_mask_buffer(handle, R - 2, mask=False)
+    assert ep.low_latency_query_mask_buffer(handle).cpu().numpy().tolist() == m_comb.tolist()
+    y = _expert_outputs((E, R * T, H), seed=c + 71)
+    w = to_dev(d["topk_weights"])
+    ref_out, _ = oracle.ll_combine(y, ref["slot_map"], d["topk_weights"], rank_mask=m_comb, R=R)
+    out = ep.low_latency_combine(to_dev_bf16(y), w, handle, status=st)
+    assert np.array_equal(u16(out), ref_out)
+    out2, hook2 = ep.low_latency_combine(to_dev_bf16(y), w, handle, status=st, return_recv_hook=True)
+    hook2()
+    assert np.array_equal(u16(out2), ref_out)
+    # tokens of a masked source rank combine to +0
+    toks = np.arange(N).reshape(R, n_s)[[1, 2]].reshape(-1)
+    assert np.all(u16(out)[toks] == 0)
     assert status_value(st) == 0
