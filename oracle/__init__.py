@@ -30,7 +30,9 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # EP_ORACLE_LIB: a prebuilt oracle library to load instead (the
+        # mutation test points it at deliberately broken copies).
+        path = os.environ.get("EP_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         P = ctypes.c_void_p
         i32, i64 = ctypes.c_int, ctypes.c_int64

@@ -184,3 +184,24 @@ def test_ue8m0_bytes_decode_to_the_scale_and_clamp_tiny_blocks():
     q, s = oracle.quantize_rows(tiny, round_scale=True)
     assert s[0, 0] < 2.0 ** -127
     assert oracle.ue8m0_from_scales(np.zeros(3, np.float32)).tolist() == [0, 0, 0]
+
+
+def test_quantisation_divides_by_the_scale():
+    # The reading q = e4m3(x / s) with one IEEE fp32 division ("DeepEP V1
+    # guide" 5.2(6) gives only the scale's shape). For these BF16 (x, amax)
+    # pairs, found by a numpy search, multiplying by fl(1/s) or by
+    # fl(448/amax) instead lands on a neighbouring code, so this pins the
+    # division itself.
+    for x_bits, amax_bits in [(0x3C2F, 0x3CC4), (0x3C1C, 0x3D50), (0x3C3A, 0x3DF8)]:
+        row = np.zeros((1, 128), np.uint16)
+        row[0, 0], row[0, 1] = amax_bits, x_bits
+        q, s = oracle.quantize_rows(row)
+        x = np.array([x_bits << 16], np.uint32).view(np.float32)[0]
+        amax = np.array([amax_bits << 16], np.uint32).view(np.float32)[0]
+        s32 = np.float32(amax) / np.float32(448.0)
+        assert s[0, 0] == s32
+        by_div = nearest_e4m3(np.array([x / s32], np.float32))[0]
+        by_rcp = nearest_e4m3(np.array([x * (np.float32(1.0) / s32)], np.float32))[0]
+        by_448 = nearest_e4m3(np.array([x * (np.float32(448.0) / amax)], np.float32))[0]
+        assert by_div != by_rcp and by_div != by_448
+        assert q[0, 1] == by_div and q[0, 0] == 0x7E
