@@ -113,7 +113,7 @@ const char* ep_error_string(int c) {
     if (c & EP_ST_TIMEOUT) return "status: bounded in-kernel wait timed out";
     if (c & EP_ST_NOT_SENT) return "status: low-latency receive/combine without a send";
     if (c & EP_ST_MISMATCH) return "status: low-latency shapes differ from the send";
-    if (c & EP_ST_WORKSPACE) return "status: workspace barrier words not zero on entry (zero-fill it)";
+    if (c & EP_ST_WORKSPACE) return "status: workspace barrier count not zero on entry (zero-fill it)";
   }
   return "unknown code";
 }
@@ -133,6 +133,7 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
   if (N > 0 && (!L->is_token_in_rank || !L->rank_slot || !L->expert_slot)) return EP_ERR_INVALID_ARG;
   const LayoutWs w = layout_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EP_ERR_ALIGNMENT;
   int G = layout_ctas_wanted(N, K);
   const int gmax = layout_max_ctas(E, R, true);
   if (gmax < 1) return EP_ERR_UNSUPPORTED;
@@ -331,6 +332,7 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   if (!aligned16(x) || !aligned16(recv_x) || (use_fp8 && !aligned16(recv_scales))) return EP_ERR_ALIGNMENT;
   const LLWs w = ll_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return EP_ERR_ALIGNMENT;
   const int gmax = layout_max_ctas(E, R, false);
   if (gmax < 1 || R > gmax) return EP_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

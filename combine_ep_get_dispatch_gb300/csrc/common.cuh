@@ -140,32 +140,40 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 }
 
 // ---- grid-wide barrier (cooperative launches only) --------------------------
-// One barrier per launch over two words that are zero when the launch
-// starts: bar[0] counts arrivals, bar[1] departures. The last block to leave
-// sets both back to zero (every block has stopped reading bar[0] by then),
-// so the next launch finds them cleared without a separate reset. A block
-// whose arrival count comes back >= nblocks found non-zero words (a
-// workspace that was never zero-filled, or one a timed-out launch left
-// behind): it flags EP_ST_WORKSPACE. The wait is bounded: on expiry it flags
-// EP_ST_TIMEOUT and lets the block go on.
-__device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, int32_t* status) {
+// One barrier per launch over two words that persist across launches: bar[0]
+// counts arrivals and is zero between launches, bar[1] is a generation
+// number. Thread 0 of every block reads the generation early in the launch
+// (barrier_generation), before it can change; the last block to arrive
+// clears the count and then bumps the generation, which releases the others.
+// So a workspace that was zero-filled once needs no reset between calls. A
+// block whose arrival count comes back >= nblocks found leftover words (a
+// workspace never zero-filled, or one an aborted launch left behind): it
+// flags EP_ST_WORKSPACE and does not wait. Waits are bounded: on expiry the
+// block flags EP_ST_TIMEOUT and goes on.
+__device__ __forceinline__ unsigned barrier_generation(const unsigned* bar) { return ld_acquire_u32(bar + 1); }
+
+__device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, unsigned gen0, int32_t* status) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(&bar[0], 1u) >= nblocks) flag(status, EP_ST_WORKSPACE);
-    unsigned spins = 0;
-    while (ld_acquire_u32(&bar[0]) < nblocks) {
-      if (++spins > kSpinLimit) {
-        flag(status, EP_ST_TIMEOUT);
-        break;
-      }
-      __nanosleep(64);
-    }
-    __threadfence();
-    if (atomicAdd(&bar[1], 1u) == nblocks - 1) {
+    __threadfence();  // this block's writes are visible before its arrival
+    const unsigned old = atomicAdd(&bar[0], 1u);
+    if (old >= nblocks) {
+      flag(status, EP_ST_WORKSPACE);
+    } else if (old == nblocks - 1) {
       atomicExch(&bar[0], 0u);
-      atomicExch(&bar[1], 0u);
+      __threadfence();
+      atomicAdd(&bar[1], 1u);
+    } else {
+      unsigned spins = 0;
+      while (ld_acquire_u32(bar + 1) == gen0) {
+        if (++spins > kSpinLimit) {
+          flag(status, EP_ST_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
+      }
     }
+    __threadfence();
   }
   __syncthreads();
 }

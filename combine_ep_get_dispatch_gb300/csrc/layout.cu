@@ -147,11 +147,13 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   int32_t* tot = base + C;             // [C]: totals, then their exclusive scan
   int32_t* own = tot + C;              // [C]: this chunk's own count
   int32_t* tmp = own + C;              // [32]
-  const int PS = max(NT, C);
+  const int PS = max(4 * NT, C);      // >= P * C for either prefix path below
   int32_t* part = tmp + 32;            // [2][PS]: partial sums over chunks
   int32_t* scode = part + 2 * PS;      // [tokens_per_cta * K]: entry codes (kStaged)
 
   bool bad = false;
+  // The barrier's generation, read before any block can have arrived.
+  const unsigned gen0 = (G > 1 && tid == 0) ? barrier_generation(p.ws_barrier) : 0u;
   // Low-latency shrink mode: a masked source rank sends nothing (this CTA's
   // chunk is that rank's tokens).
   const bool src_masked = kLL && p.rank_mask && __ldg(p.rank_mask + cta) != 0;
@@ -226,14 +228,41 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     }
   }
   if (G > 1)
-    grid_barrier(p.ws_barrier, static_cast<unsigned>(G), p.status);
+    grid_barrier(p.ws_barrier, static_cast<unsigned>(G), gen0, p.status);
   else
     __syncthreads();
 
   // Prefix over earlier chunks and totals over all chunks. P threads share a
-  // column, each summing every P-th chunk with 8 loads in flight.
-  const int P = max(1, min(NT / C, G));
-  for (int j = tid; j < P * C; j += NT) {
+  // column (four columns when C % 4 == 0: 16-byte loads), each summing every
+  // P-th chunk with all of its loads in flight at once.
+  const int CV = (C % 4 == 0) ? C / 4 : 0;   // 16-byte column groups
+  const int P = CV ? max(1, min(NT / CV, G)) : max(1, min(NT / C, G));
+  if (CV) {
+    const int4* chunk4 = reinterpret_cast<const int4*>(p.ws_chunk);
+    for (int j = tid; j < P * CV; j += NT) {
+      const int cv = j % CV, pp = j / CV;
+      int4 pre = make_int4(0, 0, 0, 0), total = pre;
+      for (int c = pp; c < G; c += 8 * P) {
+        int4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = (c + u * P < G) ? __ldcg(chunk4 + static_cast<int64_t>(c + u * P) * CV + cv) : make_int4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const bool before = c + u * P < cta;
+          pre.x += before ? v[u].x : 0; pre.y += before ? v[u].y : 0;
+          pre.z += before ? v[u].z : 0; pre.w += before ? v[u].w : 0;
+          total.x += v[u].x; total.y += v[u].y; total.z += v[u].z; total.w += v[u].w;
+        }
+      }
+      const int col = 4 * cv;  // part[pp * C + col .. col + 3]
+      part[pp * C + col] = pre.x; part[pp * C + col + 1] = pre.y;
+      part[pp * C + col + 2] = pre.z; part[pp * C + col + 3] = pre.w;
+      part[PS + pp * C + col] = total.x; part[PS + pp * C + col + 1] = total.y;
+      part[PS + pp * C + col + 2] = total.z; part[PS + pp * C + col + 3] = total.w;
+    }
+  }
+  for (int j = tid; !CV && j < P * C; j += NT) {
     const int col = j % C, pp = j / C;
     int pre = 0, total = 0, c = pp;
     for (; c + 7 * P < G; c += 8 * P) {
@@ -348,6 +377,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kHistBudget = 96 * 1024;    // per-warp counters
 
 // Threads per block: as many warps (up to 32) as the per-warp counters allow.
+// (Fewer warps for small chunks were measured slower on a 128-token batch.)
 static int layout_threads(int E, int R, bool with_rank) {
   const size_t C = static_cast<size_t>(E) + (with_rank ? R : 0);
   int W = 32;
@@ -359,7 +389,7 @@ static size_t layout_smem(int E, int R, bool with_rank, int threads, size_t stag
   const size_t C = static_cast<size_t>(E) + (with_rank ? R : 0);
   const size_t CP = C | 1;
   const size_t W = threads / 32;
-  const size_t PS = C > static_cast<size_t>(threads) ? C : static_cast<size_t>(threads);
+  const size_t PS = C > 4 * static_cast<size_t>(threads) ? C : 4 * static_cast<size_t>(threads);
   return sizeof(int32_t) * (W * CP + 3 * C + 32 + 2 * PS + staged_entries);
 }
 

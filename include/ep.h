@@ -61,7 +61,7 @@ extern "C" {
 #define EP_ST_TIMEOUT 0x8     /* a bounded in-kernel wait gave up */
 #define EP_ST_NOT_SENT 0x10   /* low-latency receive without a matching send */
 #define EP_ST_MISMATCH 0x20   /* low-latency shapes differ from those of the send */
-#define EP_ST_WORKSPACE 0x40  /* the workspace's barrier words were not zero on entry */
+#define EP_ST_WORKSPACE 0x40  /* the workspace's barrier count was not zero on entry */
 
 /* ---- dispatch payload flags (the `fp8_flags` / `use_fp8` arguments) -------
  * 0: BF16 rows. EP_FP8: E4M3 rows with one fp32 scale per 128 channels,
@@ -173,7 +173,7 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, 
  *
  *   L          handle: sizes, topk_idx and the output arrays (see ep_layout_t)
  *   workspace  device scratch of at least ep_layout_workspace_bytes(...)
- *              bytes, zero-filled before its first use (cudaMemset once at
+ *              bytes, 16-byte aligned, zero-filled before its first use (cudaMemset once at
  *              allocation). Every call leaves it as it needs to find it
  *              next time, so it is not cleared again between calls. Must
  *              not be used by another call in flight.
@@ -345,7 +345,7 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *   recv_x       [E, R*T, hidden] BF16, or E4M3 with EP_FP8
  *   recv_scales  [E, R*T, hidden/128] fp32, or UE8M0 bytes (FP8 only)
  *   recv_src     [E, R*T] int32: global token index of each written row
- *   workspace    at least ep_ll_workspace_bytes(...) bytes, zero-filled
+ *   workspace    at least ep_ll_workspace_bytes(...) bytes, 16-byte aligned, zero-filled
  *                before its first use (as for ep_get_dispatch_layout: each
  *                send leaves its barrier words zero again); afterwards it
  *                holds the routing that receive and combine use, until the

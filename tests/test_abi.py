@@ -69,6 +69,8 @@ def test_host_validation_rejects_before_cuda(L):
     # workspace too small
     lay = ep.ep_layout_t(10, 8, 256, 8, P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16))
     assert L.ep_get_dispatch_layout(ctypes.byref(lay), P(256), 16, None, None) == ep.EP_ERR_WORKSPACE
+    # workspace not 16-byte aligned
+    assert L.ep_get_dispatch_layout(ctypes.byref(lay), P(264), 1 << 20, None, None) == ep.EP_ERR_ALIGNMENT
     # dispatch: misaligned x, bad hidden sizes
     assert L.ep_dispatch(ctypes.byref(lay), P(18), 64, 0, None, None, None, None, None) == ep.EP_ERR_ALIGNMENT
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 60, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
