@@ -157,8 +157,13 @@ def _p(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
+        if _raw_stream is not None:   # the current stream's handle without building a Stream object
+            return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
@@ -178,13 +183,17 @@ class Layout:
     rank_slot: torch.Tensor
     expert_slot: torch.Tensor
     expert_alignment: int = 1
+    _c: Optional[ep_layout_t] = dataclasses.field(default=None, init=False, repr=False, compare=False)
 
     def c_struct(self) -> ep_layout_t:
-        N, K = self.topk_idx.shape
-        return ep_layout_t(N, K, self.num_experts, self.num_ranks, _p(self.topk_idx),
-                           _p(self.num_tokens_per_rank), _p(self.num_tokens_per_expert),
-                           _p(self.is_token_in_rank), _p(self.rank_offset), _p(self.expert_offset),
-                           _p(self.rank_slot), _p(self.expert_slot), int(self.expert_alignment))
+        """The C handle, built once: a Layout's arrays are fixed when it is made."""
+        if self._c is None:
+            N, K = self.topk_idx.shape
+            self._c = ep_layout_t(N, K, self.num_experts, self.num_ranks, _p(self.topk_idx),
+                                  _p(self.num_tokens_per_rank), _p(self.num_tokens_per_expert),
+                                  _p(self.is_token_in_rank), _p(self.rank_offset), _p(self.expert_offset),
+                                  _p(self.rank_slot), _p(self.expert_slot), int(self.expert_alignment))
+        return self._c
 
     @property
     def num_recv_tokens_per_expert_list(self) -> torch.Tensor:

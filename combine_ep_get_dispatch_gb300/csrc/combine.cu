@@ -142,9 +142,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   // One block per token (the hardware scheduler hands blocks to SMs as they
   // free up); a batch with fewer tokens than eight blocks per SM splits each
   // row into up to nvec / 128 spans.
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms(current_device());
   const int nvec = p.H / 8;
   int nchunk = 1;
   const int64_t want = static_cast<int64_t>(sms) * 8;

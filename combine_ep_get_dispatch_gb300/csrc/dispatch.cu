@@ -344,8 +344,7 @@ cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s) {
   const int wpb = kF8Threads / 32;
   const size_t smem = static_cast<size_t>(wpb) * f8_warp_bytes(p.H);
   const void* fn = reinterpret_cast<const void*>(&dispatch_fp8_kernel);
-  const cudaError_t err =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const cudaError_t err = ensure_dynamic_smem(fn, current_device(), smem);
   if (err != cudaSuccess) return err;
   const int64_t grid = (p.N + wpb - 1) / wpb;
   dispatch_fp8_kernel<<<static_cast<unsigned>(grid), kF8Threads, smem, s>>>(p);
@@ -355,9 +354,8 @@ cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s) {
 cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
   const WarpSmem ws = warp_smem(p.H);
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int dev = current_device();
+  const int sms = device_sms(dev);
   // Up to 4 warps per CTA; a batch with fewer tokens than 4 per SM uses
   // fewer, so its rows spread over more SMs (and their copy engines).
   int W = kMaxWarps;
@@ -366,10 +364,9 @@ cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s) {
   while (W > 1 && kBarBytes + W * ws.per_warp > budget) --W;
   const size_t smem = kBarBytes + static_cast<size_t>(W) * ws.per_warp;
   const void* fn = reinterpret_cast<const void*>(&dispatch_bf16_kernel);
-  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const cudaError_t err = ensure_dynamic_smem(fn, dev, smem);
   if (err != cudaSuccess) return err;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, W * 32, smem);
-  if (err != cudaSuccess) return err;
+  const int per_sm = blocks_per_sm(fn, dev, W * 32, smem);
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t need = (p.N + W - 1) / W;
   const int64_t full = static_cast<int64_t>(per_sm) * sms;

@@ -135,6 +135,15 @@ struct LLRecvParams {
   int32_t* status;
 };
 
+// Host-side launch bookkeeping, asked of the runtime once per process
+// (launch_cache.cu). current_device() is -1 on failure; the others return 0 /
+// false on failure.
+int current_device();
+int device_sms(int dev);
+bool device_cooperative(int dev);
+cudaError_t ensure_dynamic_smem(const void* fn, int dev, size_t smem);  // raise the kernel's limit to >= smem
+int blocks_per_sm(const void* fn, int dev, int threads, size_t smem);   // occupancy, 0 on failure
+
 // Launchers: return cudaSuccess or the launch error.
 size_t layout_smem_bytes(int E, int R, bool with_rank);
 int layout_max_ctas(int E, int R, bool with_rank);  // co-resident limit (device-specific)

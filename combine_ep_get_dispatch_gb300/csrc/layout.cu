@@ -373,7 +373,6 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
 // ---- host side ---------------------------------------------------------------
 constexpr size_t kMaxStagedEntries = 24576;  // 96 KB of entry codes per CTA
 constexpr int kVariants = 8;                 // kRank x kLL x kStaged
-constexpr int kMaxDevices = 64;
 constexpr size_t kHistBudget = 96 * 1024;    // per-warp counters
 
 // Threads per block: as many warps (up to 32) as the per-warp counters allow.
@@ -411,35 +410,18 @@ static const void* layout_fn(bool rank, bool ll, bool staged) {
   return fns[(rank ? 4 : 0) + (ll ? 2 : 0) + (staged ? 1 : 0)];
 }
 
-// Raise each variant's dynamic shared memory limit once per device.
-static bool g_attr_set[kMaxDevices][kVariants];
-
-static cudaError_t prepare(int dev, bool rank, bool ll, bool staged) {
-  const int v = (rank ? 4 : 0) + (ll ? 2 : 0) + (staged ? 1 : 0);
-  if (dev >= 0 && dev < kMaxDevices && g_attr_set[dev][v]) return cudaSuccess;
-  int optin = 0;
-  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const cudaError_t err = cudaFuncSetAttribute(layout_fn(rank, ll, staged),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (err == cudaSuccess && dev >= 0 && dev < kMaxDevices) g_attr_set[dev][v] = true;
-  return err;
+static cudaError_t prepare(int dev, bool rank, bool ll, bool staged, size_t smem) {
+  return ensure_dynamic_smem(layout_fn(rank, ll, staged), dev, smem);
 }
 
 static int coresident(int dev, bool rank, bool ll, bool staged, int threads, size_t smem) {
-  int sms = 0, per_sm = 0;
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (prepare(dev, rank, ll, staged) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_fn(rank, ll, staged), threads, smem) !=
-      cudaSuccess)
-    return 0;
-  return per_sm * sms;
+  if (prepare(dev, rank, ll, staged, smem) != cudaSuccess) return 0;
+  return blocks_per_sm(layout_fn(rank, ll, staged), dev, threads, smem) * device_sms(dev);
 }
 
 int layout_max_ctas(int E, int R, bool with_rank) {
-  int dev = 0, coop = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  if (!coop) return 0;
+  const int dev = current_device();
+  if (dev < 0 || !device_cooperative(dev)) return 0;
   const int threads = layout_threads(E, R, with_rank);
   const size_t smem = layout_smem(E, R, with_rank, threads, 0);
   const int a = coresident(dev, with_rank, false, false, threads, smem);
@@ -448,9 +430,8 @@ int layout_max_ctas(int E, int R, bool with_rank) {
 }
 
 cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll, cudaStream_t s) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorNoDevice;
   const int threads = layout_threads(p.E, p.R, with_rank);
   const size_t entries = static_cast<size_t>(p.tokens_per_cta) * p.K;
   bool staged = entries <= kMaxStagedEntries;
@@ -459,7 +440,7 @@ cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll,
     staged = false;
     smem = layout_smem(p.E, p.R, with_rank, threads, 0);
   }
-  err = prepare(dev, with_rank, ll, staged);
+  const cudaError_t err = prepare(dev, with_rank, ll, staged, smem);
   if (err != cudaSuccess) return err;
   LayoutParams q = p;
   q.magic_L = p.L > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + p.L - 1) / p.L) : 0u;

@@ -88,9 +88,7 @@ cudaError_t launch_ll_mask(int32_t* mask, int R, int mode, int rank, int value, 
 
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms(current_device());
   const int64_t blocks = (n + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   e4m3_encode_kernel<<<static_cast<int>(blocks < cap ? blocks : cap), 256, 0, s>>>(in, out, n);
