@@ -150,7 +150,13 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 // workspace never zero-filled, or one an aborted launch left behind): it
 // flags EP_ST_WORKSPACE and does not wait. Waits are bounded: on expiry the
 // block flags EP_ST_TIMEOUT and goes on.
-__device__ __forceinline__ unsigned barrier_generation(const unsigned* bar) { return ld_acquire_u32(bar + 1); }
+// A relaxed read: the generation cannot change before this block arrives, so
+// no ordering is needed, and the thread does not stall on it until the wait.
+__device__ __forceinline__ unsigned barrier_generation(const unsigned* bar) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar + 1));
+  return v;
+}
 
 __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, unsigned gen0, int32_t* status) {
   __syncthreads();

@@ -158,12 +158,6 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   // chunk is that rank's tokens).
   const bool src_masked = kLL && p.rank_mask && __ldg(p.rank_mask + cta) != 0;
   for (int i = tid; i < W * CP; i += NT) hist[i] = 0;
-  if (kRank) {
-    for (int64_t i = t0 * R + tid; i < t1 * R; i += NT) {
-      p.mask[i] = 0;
-      p.rank_slot[i] = -1;
-    }
-  }
   if (kStaged) {
     // One coalesced pass over the chunk's indices; each entry's rank is
     // computed once here, the first-on-rank flags per token after it.
@@ -231,6 +225,15 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     grid_barrier(p.ws_barrier, static_cast<unsigned>(G), gen0, p.status);
   else
     __syncthreads();
+  // Clear this chunk's rows of the mask and the rank slots now, after the
+  // barrier (whose fence then need not wait for these stores); the block
+  // synchronisations below order them before pass 2 writes its entries.
+  if (kRank) {
+    for (int64_t i = t0 * R + tid; i < t1 * R; i += NT) {
+      p.mask[i] = 0;
+      p.rank_slot[i] = -1;
+    }
+  }
 
   // Prefix over earlier chunks and totals over all chunks. P threads share a
   // column (four columns when C % 4 == 0: 16-byte loads), each summing every
