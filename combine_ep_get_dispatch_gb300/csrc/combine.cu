@@ -47,12 +47,13 @@ __device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b)
 // low-latency combine).
 template <bool kGather>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int nchunk) {
-  extern __shared__ int32_t s_dyn[];  // K rows, then K weights
-  __shared__ int s_ok;
-  const int tid = threadIdx.x;
+  extern __shared__ int32_t s_dyn[];  // the token's routed slots, in order: rows, weights, slot index
+  __shared__ int s_ok, s_nv;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K, H = p.H;
   int32_t* s_row = s_dyn;
   float* s_w = reinterpret_cast<float*>(s_dyn + K);
+  int32_t* s_k = s_dyn + 2 * K;
   if (p.ll_hdr) {
     if (tid == 0) {
       const LLHeader h = *p.ll_hdr;
@@ -75,45 +76,56 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int64_t t = it / nchunk;
     const int v0 = static_cast<int>(it - t * nchunk) * span;
     const int v1 = min(nvec, v0 + span);
-    for (int k = tid; k < K; k += kThreads) {
-      int32_t row = __ldg(p.slot + t * K + k);
-      // Low-latency shrink mode: skip the slots of ranks masked now (the
-      // expert's rank, from its region e = row / (R*T), or the token's source).
-      if (row >= 0 && p.rank_mask &&
-          (__ldg(p.rank_mask + static_cast<int>(row / p.ll_cap) / p.ll_L) != 0 ||
-           __ldg(p.rank_mask + static_cast<int>(t / p.ll_ns)) != 0))
-        row = -1;
-      if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + k);
-      if (row >= p.y_rows) {
-        flag(p.status, EP_ST_CAPACITY);
-        row = -1;
+    // Warp 0 lists the routed slots in slot order (masked ones dropped), so
+    // every row load below is useful and all of them go out in one round
+    // whenever a token has at most kChunk routed slots.
+    if (tid < 32) {
+      int nv = 0;
+      for (int k0 = 0; k0 < K; k0 += 32) {
+        const int k = k0 + lane;
+        int32_t row = k < K ? __ldg(p.slot + t * K + k) : -1;
+        // Low-latency shrink mode: skip the slots of ranks masked now (the
+        // expert's rank, from its region e = row / (R*T), or the token's source).
+        if (row >= 0 && p.rank_mask &&
+            (__ldg(p.rank_mask + static_cast<int>(row / p.ll_cap) / p.ll_L) != 0 ||
+             __ldg(p.rank_mask + static_cast<int>(t / p.ll_ns)) != 0))
+          row = -1;
+        if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + k);
+        if (row >= p.y_rows) {
+          flag(p.status, EP_ST_CAPACITY);
+          row = -1;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, row >= 0);
+        if (row >= 0) {
+          const int pos = nv + __popc(m & lanemask_lt());
+          s_row[pos] = row;
+          s_w[pos] = p.w ? __ldg(p.w + t * K + k) : 1.0f;
+          s_k[pos] = k;
+        }
+        nv += __popc(m);
       }
-      s_row[k] = row;
-      s_w[k] = p.w ? __ldg(p.w + t * K + k) : 1.0f;
+      if (lane == 0) s_nv = nv;
     }
     __syncthreads();
+    const int nv = s_nv;
     for (int v = v0 + tid; v < v1; v += kThreads) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      for (int k0 = 0; k0 < K; k0 += kChunk) {
+      for (int i0 = 0; i0 < nv; i0 += kChunk) {
         uint4 yv[kChunk];
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j) {
-          const int k = k0 + j;
-          const int32_t row = (k < K) ? s_row[k] : -1;
-          if (row >= 0)
-            yv[j] = ld_stream_v4(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
-        }
+        for (int j = 0; j < kChunk; ++j)
+          if (i0 + j < nv)
+            yv[j] = ld_stream_v4(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(s_row[i0 + j]) * H) + v);
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) {
-          const int k = k0 + j;
-          const int32_t row = (k < K) ? s_row[k] : -1;
-          if (row < 0) continue;
+          const int i = i0 + j;
+          if (i >= nv) break;
           if (kGather)
-            reinterpret_cast<uint4*>(p.out + (t * K + k) * H)[v] = yv[j];
+            reinterpret_cast<uint4*>(p.out + (t * K + s_k[i]) * H)[v] = yv[j];
           else
-            fma8(acc, s_w[k], yv[j]);
+            fma8(acc, s_w[i], yv[j]);
         }
       }
       if (kGather) continue;
@@ -155,7 +167,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(p.N) * nchunk;
   const int64_t cap = int64_t(1) << 30;
   const int grid = static_cast<int>(items < cap ? items : cap);
-  const size_t smem = static_cast<size_t>(p.K) * 8;
+  const size_t smem = static_cast<size_t>(p.K) * 12;
   if (p.gather)
     combine_kernel<true><<<grid, kThreads, smem, s>>>(p, nchunk);
   else
@@ -168,7 +180,8 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
 // over k ascending whose expert lives on r of w[t, k] * y[expert_slot[t, k]] )
 // (the reduction DeepEP's expert layer does on each rank before combine).
 // One block per token; the K slots are grouped by rank in shared memory and
-// each rank's chain runs in slot order.
+// each rank's chain runs in slot order (for K <= 8 from registers, after one
+// round of loads of all the token's rows).
 __global__ void __launch_bounds__(kThreads) combine_to_ranks_kernel(const CombineRanksParams p) {
   __shared__ int32_t s_row[EP_MAX_TOPK], s_rank[EP_MAX_TOPK], s_out[EP_MAX_TOPK];
   __shared__ float s_w[EP_MAX_TOPK];
@@ -199,6 +212,40 @@ __global__ void __launch_bounds__(kThreads) combine_to_ranks_kernel(const Combin
       s_out[tid] = orow;
     }
     __syncthreads();
+    if (K <= kChunk) {
+      // All of the token's rows are loaded at once for a vector; each rank's
+      // chain then runs from registers, in slot order.
+      for (int v = tid; v < nvec; v += kThreads) {
+        uint4 yv[kChunk];
+#pragma unroll
+        for (int k = 0; k < kChunk; ++k)
+          if (k < K && s_rank[k] >= 0)
+            yv[k] = ld_stream_v4(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(s_row[k]) * H) + v);
+#pragma unroll
+        for (int k0 = 0; k0 < kChunk; ++k0) {
+          if (k0 >= K) break;
+          const int r = s_rank[k0];
+          if (r < 0 || s_out[k0] < 0) continue;
+          bool first = true;
+          for (int k = 0; k < k0; ++k) first &= s_rank[k] != r;
+          if (!first) continue;
+          float acc[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+          for (int k = 0; k < kChunk; ++k)
+            if (k >= k0 && k < K && s_rank[k] == r) fma8(acc, s_w[k], yv[k]);
+          uint4 o;
+          o.x = pack_bf16x2(acc[0], acc[1]);
+          o.y = pack_bf16x2(acc[2], acc[3]);
+          o.z = pack_bf16x2(acc[4], acc[5]);
+          o.w = pack_bf16x2(acc[6], acc[7]);
+          reinterpret_cast<uint4*>(p.rank_out + static_cast<int64_t>(s_out[k0]) * H)[v] = o;
+        }
+      }
+      __syncthreads();
+      continue;
+    }
     for (int k0 = 0; k0 < K; ++k0) {
       const int r = s_rank[k0];
       if (r < 0) continue;
