@@ -312,6 +312,18 @@ __global__ void __launch_bounds__(kThreads) combine_backward_kernel(const Combin
       for (int j = 0; j < kChunk; ++j) dot[j] = 0.0f;
       for (int v = tid; v < nvec; v += kThreads) {
         const uint4 g = __ldg(g_row + v);
+        // All of this chunk's row loads go out first (before the gradient
+        // stores, which the compiler could not move loads across).
+        uint4 yv_all[kChunk];
+        if (p.grad_w && p.y) {
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) {
+            const int k = k0 + j;
+            const int32_t row = (k < K) ? s_row[k] : -1;
+            if (row >= 0)
+              yv_all[j] = ld_stream_v4(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
+          }
+        }
         const float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
                              bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
 #pragma unroll
@@ -329,7 +341,7 @@ __global__ void __launch_bounds__(kThreads) combine_backward_kernel(const Combin
             reinterpret_cast<uint4*>(p.grad_y + static_cast<int64_t>(row) * H)[v] = o;
           }
           if (p.grad_w && p.y) {
-            const uint4 yv = __ldg(reinterpret_cast<const uint4*>(p.y + static_cast<int64_t>(row) * H) + v);
+            const uint4 yv = yv_all[j];
             dot[j] = __fmaf_rn(gf[0], bf16_lo(yv.x), dot[j]);
             dot[j] = __fmaf_rn(gf[1], bf16_hi(yv.x), dot[j]);
             dot[j] = __fmaf_rn(gf[2], bf16_lo(yv.y), dot[j]);

@@ -379,30 +379,33 @@ cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s) {
 
 // Zero the padding rows of an aligned expert-major buffer: rows
 // [expert_off[e] + count[e], expert_off[e+1]) of each expert e (payload,
-// scales, src = -1). One block per expert.
+// scales, src = -1). Block (e, s) writes the s-th of kPadSlices interleaved
+// shares of expert e's padding, so the work spreads over the whole GPU.
+constexpr int kPadSlices = 8;
+
 __global__ void __launch_bounds__(256) pad_zero_kernel(const PadParams p) {
   const int e = blockIdx.x;
   const int64_t lo = static_cast<int64_t>(__ldg(p.expert_off + e)) + __ldg(p.per_expert + e);
   int64_t hi = __ldg(p.expert_off + e + 1);
   if (hi > p.cap) {
-    if (threadIdx.x == 0) flag(p.status, EP_ST_CAPACITY);
+    if (threadIdx.x == 0 && blockIdx.y == 0) flag(p.status, EP_ST_CAPACITY);
     hi = p.cap;
   }
   if (hi <= lo) return;
+  const int64_t first = static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x;
+  const int64_t step = static_cast<int64_t>(gridDim.y) * blockDim.x;
   const int64_t vpr = p.row_bytes / 16;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int64_t i = threadIdx.x; i < (hi - lo) * vpr; i += blockDim.x)
-    reinterpret_cast<uint4*>(p.x + lo * p.row_bytes)[i] = z;
+  for (int64_t i = first; i < (hi - lo) * vpr; i += step) reinterpret_cast<uint4*>(p.x + lo * p.row_bytes)[i] = z;
   if (p.scales)
-    for (int64_t i = threadIdx.x; i < (hi - lo) * p.scale_row_bytes; i += blockDim.x)
-      p.scales[lo * p.scale_row_bytes + i] = 0;
+    for (int64_t i = first; i < (hi - lo) * p.scale_row_bytes; i += step) p.scales[lo * p.scale_row_bytes + i] = 0;
   if (p.src)
-    for (int64_t r = lo + threadIdx.x; r < hi; r += blockDim.x) p.src[r] = -1;
+    for (int64_t r = lo + first; r < hi; r += step) p.src[r] = -1;
 }
 
 cudaError_t launch_pad_zero(const PadParams& p, cudaStream_t s) {
   if (p.E <= 0) return cudaSuccess;
-  pad_zero_kernel<<<p.E, 256, 0, s>>>(p);
+  pad_zero_kernel<<<dim3(p.E, kPadSlices), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
