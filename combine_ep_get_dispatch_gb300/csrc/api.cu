@@ -367,7 +367,7 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   dp.exp_src_is_token = 1;
   dp.overflow_bit = EP_ST_LL_OVERFLOW;
   dp.status = status;
-  return cuda_rc(launch_dispatch(dp, use_fp8 != 0, s));
+  return cuda_rc(launch_dispatch(dp, use_fp8 != 0, s, /*after_layout=*/true));
 }
 
 int ep_ll_dispatch_recv(void* workspace, size_t workspace_bytes, int N, int K, int E, int R, int T,

@@ -139,6 +139,16 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it on the stream is still running, once every block of
+// that kernel has issued launch_dependents (or exited). Before it reads what
+// that kernel writes it must wait for it: grid_dependency_wait returns once
+// the preceding grid has completed and its memory is visible. In a launch
+// without the attribute the wait returns at once.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- grid-wide barrier (cooperative launches only) --------------------------
 // One barrier per launch over two words that persist across launches: bar[0]
 // counts arrivals and is zero between launches, bar[1] is a generation

@@ -149,7 +149,10 @@ size_t layout_smem_bytes(int E, int R, bool with_rank);
 int layout_max_ctas(int E, int R, bool with_rank);  // co-resident limit (device-specific)
 cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll, cudaStream_t s);
 
-cudaError_t launch_dispatch(const DispatchParams& p, bool fp8, cudaStream_t s);
+// after_layout: the kernel just before on the stream is this library's
+// layout, launched by the same call; the dispatch then starts as its
+// programmatic dependent (rows loaded and quantised while the layout runs).
+cudaError_t launch_dispatch(const DispatchParams& p, bool fp8, cudaStream_t s, bool after_layout = false);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s);
 cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s);

@@ -151,6 +151,9 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   int32_t* part = tmp + 32;            // [2][PS]: partial sums over chunks
   int32_t* scode = part + 2 * PS;      // [tokens_per_cta * K]: entry codes (kStaged)
 
+  // The low-latency send's dispatch may start now: it loads and quantises its
+  // rows, then waits for this grid to finish before it reads any slot.
+  launch_dependents();
   bool bad = false;
   // The barrier's generation, read before any block can have arrived.
   const unsigned gen0 = (G > 1 && tid == 0) ? barrier_generation(p.ws_barrier) : 0u;
