@@ -18,11 +18,14 @@ namespace ep {
 namespace {
 
 constexpr int kRecvThreads = 1024;
+constexpr int kRecvUnroll = 8;  // ranges per thread with their loads in flight together
 
-// One block (E <= 1024 = one expert per thread). Every load goes out before
-// the header has been checked: the header, this thread's count and running
-// statistic, and its first range; only the stores wait for the check. The
-// header is marked consumed last; later launches on the stream see it.
+// One block (E <= 1024 = one expert per thread). Every load of the first
+// round goes out before the header has been checked: the header, this
+// thread's count and running statistic, and up to kRecvUnroll of its ranges;
+// only the stores wait for the check. Larger range tables are copied in
+// further rounds of kRecvUnroll loads, then kRecvUnroll stores. The header is
+// marked consumed last; later launches on the stream see it.
 __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParams p, int E, int R) {
   __shared__ int s_ok;
   const int tid = threadIdx.x;
@@ -30,8 +33,14 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParam
   if (tid == 0) h = *p.hdr;  // written by an earlier launch on this stream
   const int32_t c = tid < E ? p.count[tid] : 0;
   const int32_t acc = (tid < E && p.stats) ? p.stats[tid] : 0;
-  const int64_t n = static_cast<int64_t>(E) * R;
-  const int64_t r0 = (p.layout_range && tid < n) ? p.range[tid] : 0;
+  const int64_t n = p.layout_range ? static_cast<int64_t>(E) * R : 0;
+  constexpr int64_t kRound = static_cast<int64_t>(kRecvThreads) * kRecvUnroll;
+  int64_t r[kRecvUnroll];
+#pragma unroll
+  for (int u = 0; u < kRecvUnroll; ++u) {
+    const int64_t i = static_cast<int64_t>(u) * kRecvThreads + tid;
+    r[u] = i < n ? p.range[i] : 0;
+  }
   if (tid == 0) {
     int ok = 1;
     if (h.magic != kMagicSent) {
@@ -50,9 +59,19 @@ __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParam
     p.recv_count[tid] = c;
     if (p.stats) p.stats[tid] = acc + c;  // one block: no other writer
   }
-  if (p.layout_range) {
-    if (tid < n) p.layout_range[tid] = r0;
-    for (int64_t i = tid + kRecvThreads; i < n; i += kRecvThreads) p.layout_range[i] = p.range[i];
+  for (int64_t b = 0; b < n; b += kRound) {
+    if (b > 0) {
+#pragma unroll
+      for (int u = 0; u < kRecvUnroll; ++u) {
+        const int64_t i = b + static_cast<int64_t>(u) * kRecvThreads + tid;
+        r[u] = i < n ? p.range[i] : 0;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRecvUnroll; ++u) {
+      const int64_t i = b + static_cast<int64_t>(u) * kRecvThreads + tid;
+      if (i < n) p.layout_range[i] = r[u];
+    }
   }
   __syncthreads();
   if (tid == 0) p.hdr->magic = kMagicReceived;
