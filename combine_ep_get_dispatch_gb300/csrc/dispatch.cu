@@ -38,111 +38,90 @@ __host__ __device__ inline unsigned bf16_row_bytes(int H) { return round_up(stat
 
 constexpr unsigned kBarBytes = 128;  // one mbarrier per warp
 
-// A warp per token, launched one token per warp (the loop covers any grid).
-// Lane 0 brings the row in with one bulk TMA copy completing on the warp's
-// mbarrier; every destination row then leaves by one bulk TMA store from the
-// same shared row, and the warp moves on once those stores have read it.
-// The block scheduler balances the work: a grid of one token per warp, with
-// blocks retiring as their rows leave, measured 12 % faster on the 16384-token
-// workload than a persistent grid (whose warps each own a fixed share of the
-// tokens, so the grid waits for the warp whose tokens have the most copies).
+// A warp per token, one token per warp: lane 0 brings the row in with one
+// bulk TMA copy completing on the warp's mbarrier; every destination row then
+// leaves by one bulk TMA store from the same shared row. The block scheduler
+// balances the work: with a grid of one token per warp, blocks retiring as
+// their rows leave, the 16384-token workload ran 12 % faster than on a
+// persistent grid (whose warps each own a fixed share of the tokens, so the
+// grid waits for the warp whose tokens have the most copies).
 __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const DispatchParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, W = blockDim.x >> 5;
   const int H = p.H, K = p.K, R = p.R, L = p.L, E = p.E;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * W + w;
+  if (t >= p.N) return;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + w;
   uint8_t* src = smem + kBarBytes + static_cast<size_t>(w) * bf16_row_bytes(H);
   const unsigned xbytes = static_cast<unsigned>(H) * 2u;
   const unsigned obytes = xbytes;
-
-  const int64_t N = p.N;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + w;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * W;
   if (lane == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    if (gw < N) {
-      mbar_arrive_expect_tx(bar, xbytes);
-      bulk_g2s(src, p.x + gw * H, xbytes, bar);
-    }
+    mbar_arrive_expect_tx(bar, xbytes);
+    bulk_g2s(src, p.x + t * H, xbytes, bar);
   }
   __syncwarp();
 
-  unsigned parity = 0;
-  bool pending = gw < N;  // a row load is in flight
-  for (int64_t t = gw; t < N; t += nw) {
-    // The slots come from the layout: under a programmatic dependent launch
-    // this kernel may have started before the layout finished (the row load
-    // above needs nothing from it).
-    grid_dependency_wait();
-    // This lane's top-k slot (lane < K): expert, weight and expert-major row.
-    int e_k = -1;
-    float w_k = 0.0f;
-    int32_t erow = -1;
-    if (lane < K) {
-      e_k = __ldg(p.idx + t * K + lane);
-      if (p.w) w_k = __ldg(p.w + t * K + lane);
-      if (p.exp_x) {
-        erow = __ldcg(p.expert_slot + t * K + lane);
-        if (erow >= p.exp_cap) {
-          flag(p.status, p.overflow_bit);
-          erow = -1;
-        }
-        if (erow >= 0 && p.exp_src)
-          p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
+  // The slots come from the layout: under a programmatic dependent launch
+  // this kernel may have started before the layout finished (the row load
+  // above needs nothing from it).
+  grid_dependency_wait();
+  // This lane's top-k slot (lane < K): expert, weight and expert-major row.
+  int e_k = -1;
+  float w_k = 0.0f;
+  int32_t erow = -1;
+  if (lane < K) {
+    e_k = __ldg(p.idx + t * K + lane);
+    if (p.w) w_k = __ldg(p.w + t * K + lane);
+    if (p.exp_x) {
+      erow = __ldcg(p.expert_slot + t * K + lane);
+      if (erow >= p.exp_cap) {
+        flag(p.status, p.overflow_bit);
+        erow = -1;
       }
+      if (erow >= 0 && p.exp_src)
+        p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
     }
+  }
 
-    if (!mbar_wait(bar, parity, p.status)) break;
-    parity ^= 1u;
-    pending = false;
+  if (!mbar_wait(bar, 0, p.status)) {
+    // Timed out: give the load a bounded chance to land before the block's
+    // shared memory is released (no store has been issued yet).
+    mbar_wait(bar, 0, p.status);
+    return;
+  }
 
-    // Expert-major copies.
-    if (erow >= 0) bulk_s2g(p.exp_x + static_cast<int64_t>(erow) * obytes, src, obytes);
+  // Expert-major copies.
+  if (erow >= 0) bulk_s2g(p.exp_x + static_cast<int64_t>(erow) * obytes, src, obytes);
 
-    // Per-rank copies: lane owns ranks lane, lane + 32, ...
-    if (p.rank_x) {
-      for (int r0 = 0; r0 < R; r0 += 32) {
-        const int r = r0 + lane;
-        int32_t rrow = (r < R) ? __ldcg(p.rank_slot + t * R + r) : -1;
-        if (rrow >= p.rank_cap) {
-          flag(p.status, EP_ST_CAPACITY);
-          rrow = -1;
-        }
-        if (rrow >= 0) {
-          bulk_s2g(p.rank_x + static_cast<int64_t>(rrow) * obytes, src, obytes);
-          if (p.rank_src) p.rank_src[rrow] = static_cast<int32_t>(t);
-        }
-        if (p.rank_topk_idx || p.rank_topk_w) {
-          for (int kk = 0; kk < K; ++kk) {
-            const int ek = __shfl_sync(0xffffffffu, e_k, kk);
-            const float wk = __shfl_sync(0xffffffffu, w_k, kk);
-            if (rrow >= 0) {
-              const bool here = ek >= 0 && ek < E && ek / L == r;
-              if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? ek - r * L : -1;
-              if (p.rank_topk_w) p.rank_topk_w[static_cast<int64_t>(rrow) * K + kk] = here ? wk : 0.0f;
-            }
+  // Per-rank copies: lane owns ranks lane, lane + 32, ...
+  if (p.rank_x) {
+    for (int r0 = 0; r0 < R; r0 += 32) {
+      const int r = r0 + lane;
+      int32_t rrow = (r < R) ? __ldcg(p.rank_slot + t * R + r) : -1;
+      if (rrow >= p.rank_cap) {
+        flag(p.status, EP_ST_CAPACITY);
+        rrow = -1;
+      }
+      if (rrow >= 0) {
+        bulk_s2g(p.rank_x + static_cast<int64_t>(rrow) * obytes, src, obytes);
+        if (p.rank_src) p.rank_src[rrow] = static_cast<int32_t>(t);
+      }
+      if (p.rank_topk_idx || p.rank_topk_w) {
+        for (int kk = 0; kk < K; ++kk) {
+          const int ek = __shfl_sync(0xffffffffu, e_k, kk);
+          const float wk = __shfl_sync(0xffffffffu, w_k, kk);
+          if (rrow >= 0) {
+            const bool here = ek >= 0 && ek < E && ek / L == r;
+            if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? ek - r * L : -1;
+            if (p.rank_topk_w) p.rank_topk_w[static_cast<int64_t>(rrow) * K + kk] = here ? wk : 0.0f;
           }
         }
       }
     }
-    bulk_commit();
-    // A further token (only on a grid smaller than one token per warp): its
-    // row may land once the stores above have read the staged one.
-    const int64_t tn = t + nw;
-    if (tn < N) {
-      bulk_wait_read<0>();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, xbytes);
-        bulk_g2s(src, p.x + tn * H, xbytes, bar);
-      }
-      pending = true;
-    }
   }
-  // Only after a timed-out wait can a load still be in flight: give it a
-  // bounded chance to land before the block's shared memory is released.
-  if (pending) mbar_wait(bar, parity, p.status);
+  bulk_commit();
   // The shared row must outlive the stores' reads of it.
   bulk_wait_read<0>();
 }
@@ -287,89 +266,76 @@ __global__ void __launch_bounds__(32) dispatch_fp8_kernel(const DispatchParams p
   const int lane = threadIdx.x & 31;
   const int H = p.H, K = p.K;
   const int nsc = H / 128;
+  const int64_t t = blockIdx.x;  // one token per block
+  if (t >= p.N) return;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   uint8_t* row = smem + kBarBytes;
   float* scales = reinterpret_cast<float*>(row + f8_row_bytes(H));
   int32_t* drow = reinterpret_cast<int32_t*>(scales + nsc);
-  const bool ue8m0 = p.fp8_flags & EP_FP8_UE8M0;
   const unsigned xbytes = static_cast<unsigned>(H) * 2u;
-  const int64_t N = p.N;
-  int64_t t = blockIdx.x;
   if (lane == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    if (t < N) {
-      mbar_arrive_expect_tx(bar, xbytes);
-      bulk_g2s(row, p.x + t * H, xbytes, bar);
-    }
+    mbar_arrive_expect_tx(bar, xbytes);
+    bulk_g2s(row, p.x + t * H, xbytes, bar);
   }
   __syncwarp();
-  unsigned parity = 0;
-  // One token per block (the loop covers a grid smaller than N).
-  for (; t < N; t += gridDim.x) {
-    int e_k = -1;
-    float w_k = 0.0f;
-    if (lane < K) {
-      e_k = __ldg(p.idx + t * K + lane);
-      if (p.w) w_k = __ldg(p.w + t * K + lane);
-    }
-    int ne = 0, n = 0;
-    if (!kLateDest) {
-      grid_dependency_wait();
-      n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
-    }
-    if (!mbar_wait(bar, parity, p.status)) {
-      // Timed out: give the load a bounded chance to land before the block's
-      // shared memory is released (no store has been issued yet).
-      mbar_wait(bar, parity, p.status);
-      return;
-    }
-    parity ^= 1u;
-    for (int c0 = 0; c0 < H; c0 += 512) {
-      const int c = c0 + lane * 16;
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (c < H) {
-        v0 = *reinterpret_cast<const uint4*>(row + 2 * c);
-        v1 = *reinterpret_cast<const uint4*>(row + 2 * c + 16);
-      }
-      __syncwarp();  // every lane has read this step's channels before any code overwrites them
-      float sc;
-      const uint4 q = quantize16(v0, v1, sc, p.fp8_flags);
-      if (c < H) {
-        *reinterpret_cast<uint4*>(row + c) = q;
-        if ((lane & 7) == 0) scales[c >> 7] = sc;
-      }
-    }
-    if (kLateDest) {
-      grid_dependency_wait();
-      n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    // One bulk store per destination row; lane d issues row d.
-    for (int d = lane; d < n; d += 32) {
-      uint8_t* base = d < ne ? p.exp_x : p.rank_x;
-      bulk_s2g(base + static_cast<int64_t>(drow[d]) * H, row, static_cast<unsigned>(H));
-    }
-    bulk_commit();
-    for (int d = 0; d < n; ++d) {
-      void* sbase = d < ne ? p.exp_scales : p.rank_scales;
-      if (!sbase) continue;
-      const int64_t r0 = static_cast<int64_t>(drow[d]) * nsc;
-      if (ue8m0)
-        for (int b = lane; b < nsc; b += 32) static_cast<uint8_t*>(sbase)[r0 + b] = ue8m0_byte(scales[b]);
-      else
-        for (int b = lane; b < nsc; b += 32) static_cast<float*>(sbase)[r0 + b] = scales[b];
-    }
-    // The row is reused only once the stores have read it.
-    bulk_wait_read<0>();
-    __syncwarp();
-    if (t + gridDim.x < N && lane == 0) {
-      mbar_arrive_expect_tx(bar, xbytes);
-      bulk_g2s(row, p.x + (t + gridDim.x) * H, xbytes, bar);
-    }
-    __syncwarp();
+  int e_k = -1;
+  float w_k = 0.0f;
+  if (lane < K) {
+    e_k = __ldg(p.idx + t * K + lane);
+    if (p.w) w_k = __ldg(p.w + t * K + lane);
   }
+  int ne = 0, n = 0;
+  if (!kLateDest) {
+    grid_dependency_wait();
+    n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
+  }
+  if (!mbar_wait(bar, 0, p.status)) {
+    // Timed out: give the load a bounded chance to land before the block's
+    // shared memory is released (no store has been issued yet).
+    mbar_wait(bar, 0, p.status);
+    return;
+  }
+  for (int c0 = 0; c0 < H; c0 += 512) {
+    const int c = c0 + lane * 16;
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+    if (c < H) {
+      v0 = *reinterpret_cast<const uint4*>(row + 2 * c);
+      v1 = *reinterpret_cast<const uint4*>(row + 2 * c + 16);
+    }
+    __syncwarp();  // every lane has read this step's channels before any code overwrites them
+    float sc;
+    const uint4 q = quantize16(v0, v1, sc, p.fp8_flags);
+    if (c < H) {
+      *reinterpret_cast<uint4*>(row + c) = q;
+      if ((lane & 7) == 0) scales[c >> 7] = sc;
+    }
+  }
+  if (kLateDest) {
+    grid_dependency_wait();
+    n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  // One bulk store per destination row; lane d issues row d.
+  for (int d = lane; d < n; d += 32) {
+    uint8_t* base = d < ne ? p.exp_x : p.rank_x;
+    bulk_s2g(base + static_cast<int64_t>(drow[d]) * H, row, static_cast<unsigned>(H));
+  }
+  bulk_commit();
+  const bool ue8m0 = p.fp8_flags & EP_FP8_UE8M0;
+  for (int d = 0; d < n; ++d) {
+    void* sbase = d < ne ? p.exp_scales : p.rank_scales;
+    if (!sbase) continue;
+    const int64_t r0 = static_cast<int64_t>(drow[d]) * nsc;
+    if (ue8m0)
+      for (int b = lane; b < nsc; b += 32) static_cast<uint8_t*>(sbase)[r0 + b] = ue8m0_byte(scales[b]);
+    else
+      for (int b = lane; b < nsc; b += 32) static_cast<float*>(sbase)[r0 + b] = scales[b];
+  }
+  // The shared row must outlive the stores' reads of it.
+  bulk_wait_read<0>();
 }
 
 // Launch `fn` with one DispatchParams argument; with `pdl`, as the dependent
@@ -390,16 +356,16 @@ cudaError_t launch_ex(void (*fn)(DispatchParams), unsigned grid, unsigned thread
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
-// One token per block: blocks retire as their rows leave and the block
-// scheduler hands the next tokens to the freed slots.
+// One token per block (N <= INT32_MAX fits the grid's x limit): blocks
+// retire as their rows leave and the block scheduler hands the next tokens
+// to the freed slots.
 cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s, bool pdl) {
   if (p.N <= 0) return cudaSuccess;
   const size_t smem = kBarBytes + f8_warp_bytes(p.H);
   void (*fn)(DispatchParams) = pdl ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
   if (err != cudaSuccess) return err;
-  const int64_t cap = int64_t(1) << 30;
-  return launch_ex(fn, static_cast<unsigned>(p.N < cap ? p.N : cap), 32, smem, s, pdl, p);
+  return launch_ex(fn, static_cast<unsigned>(p.N), 32, smem, s, pdl, p);
 }
 
 cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s, bool pdl) {
@@ -417,7 +383,7 @@ cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s, bool pdl) {
   void (*fn)(DispatchParams) = dispatch_bf16_kernel;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), dev, smem);
   if (err != cudaSuccess) return err;
-  // One token per warp (the grid-x limit is far above any N the ABI accepts).
+  // One token per warp (N <= INT32_MAX: the grid fits the x limit).
   const int64_t grid = (p.N + W - 1) / W;
   return launch_ex(fn, static_cast<unsigned>(grid), W * 32, smem, s, pdl, p);
 }

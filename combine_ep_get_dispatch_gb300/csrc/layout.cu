@@ -12,13 +12,14 @@
 // Design. The (token, slot) entries are cut into G contiguous chunks, one
 // per CTA (up to 32 warps), and each chunk into contiguous warp ranges. A CTA
 // first stages its chunk's indices in shared memory in one coalesced pass,
-// coding each entry as (expert, rank, first-slot-of-the-token-on-that-rank);
-// divisions by E/R and K are multiply-highs. Pass 1 counts per warp with
+// coding each entry as (expert, rank, first-slot-of-the-token-on-that-rank;
+// the flag from the token's earlier slots, neighbours of the entry's own
+// index); divisions by E/R and K are multiply-highs. Pass 1 counts per warp with
 // shared-memory atomics. A shuffle scan across warps gives each warp its
 // prefix; the chunk totals go to global memory; one bounded grid barrier
 // (cooperative launch); every CTA then sums the chunk totals before it (its
 // prefix) and all of them (the totals) and scans the totals over experts and
-// ranks. Pass 2 walks the warp's range 32 entries at a time: ballots on the
+// ranks in one pass. Pass 2 walks the warp's range 32 entries at a time: ballots on the
 // key bits give each lane the lanes with the same expert (rank), so its
 // position among them is a popcount and one leader bumps the warp's counter.
 // No atomics decide an order: slots follow (token, slot) order by
@@ -163,7 +164,9 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   for (int i = tid; i < W * CP; i += NT) hist[i] = 0;
   if (kStaged) {
     // One coalesced pass over the chunk's indices; each entry's rank is
-    // computed once here, the first-on-rank flags per token after it.
+    // computed once here. In rank mode the entry also reads its token's
+    // earlier slots (neighbours of its own index, from L1) and marks itself
+    // when it is the token's first slot on its rank.
     for (int li = tid; li < n_ent; li += NT) {
       const int e = __ldg(p.idx + a0 + li);
       int code = -1;
@@ -173,23 +176,18 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
         else
           bad = true;
       }
-      scode[li] = ll_drop<kLL>(p, code, src_masked) ? -1 : code;
-    }
-    __syncthreads();
-    if (kRank) {
-      for (int tl = tid; tl < static_cast<int>(t1 - t0); tl += NT) {
-        int32_t* row = scode + tl * K;
-        for (int k = 0; k < K; ++k) {
-          const int c = row[k];
-          if (c < 0) continue;
-          bool first = true;
-          for (int kk = 0; kk < k; ++kk) {
-            const int c2 = row[kk];
-            if (c2 >= 0 && code_r(c2) == code_r(c)) first = false;
-          }
-          if (first) row[k] = c | kFirstBit;
+      if (kRank && code >= 0) {
+        // a0 is a multiple of K, so li % K is the slot (li < 2^20 here)
+        const int k = li - fast_div(li, p.magic_K) * K;
+        bool first = true;
+#pragma unroll 4
+        for (int kk = 1; kk <= k; ++kk) {
+          const int e2 = __ldg(p.idx + a0 + li - kk);
+          if (e2 >= 0 && e2 < E && fast_div(e2, p.magic_L) == code_r(code)) first = false;
         }
+        if (first) code |= kFirstBit;
       }
+      scode[li] = ll_drop<kLL>(p, code, src_masked) ? -1 : code;
     }
   }
   __syncthreads();
@@ -209,19 +207,34 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   __syncthreads();
 
   // Per column: exclusive prefix over warps (one warp per column, lane = warp
-  // index, shuffle scan); the chunk's total goes out.
-  for (int col = w; col < C; col += W) {
-    const int v = lane < W ? hist[lane * CP + col] : 0;
-    int incl = v;
+  // index, shuffle scan); the chunk's total goes out. A warp takes its
+  // columns kScanCols at a time, their shuffle chains interleaved.
+  constexpr int kScanCols = 8;
+  for (int c0 = w; c0 < C; c0 += W * kScanCols) {
+    int v[kScanCols], incl[kScanCols];
+#pragma unroll
+    for (int j = 0; j < kScanCols; ++j) {
+      const int col = c0 + j * W;
+      v[j] = (lane < W && col < C) ? hist[lane * CP + col] : 0;
+      incl[j] = v[j];
+    }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+#pragma unroll
+      for (int j = 0; j < kScanCols; ++j) {
+        const int y = __shfl_up_sync(0xffffffffu, incl[j], o);
+        if (lane >= o) incl[j] += y;
+      }
     }
-    if (lane < W) hist[lane * CP + col] = incl - v;
-    if (lane == 31) {
-      own[col] = incl;
-      p.ws_chunk[static_cast<int64_t>(cta) * C + col] = incl;
+#pragma unroll
+    for (int j = 0; j < kScanCols; ++j) {
+      const int col = c0 + j * W;
+      if (col >= C) break;
+      if (lane < W) hist[lane * CP + col] = incl[j] - v[j];
+      if (lane == 31) {
+        own[col] = incl[j];
+        p.ws_chunk[static_cast<int64_t>(cta) * C + col] = incl[j];
+      }
     }
   }
   if (G > 1)
@@ -309,12 +322,15 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   if (p.align > 1)
     for (int e = tid; e < E; e += NT) tot[e] = (tot[e] + p.align - 1) / p.align * p.align;
   __syncthreads();
-  const int total_e = block_exclusive_scan(tot, E, tmp);
-  const int total_r = kRank ? block_exclusive_scan(tot + E, R, tmp) : 0;
+  // One scan over the expert and the rank columns together; a rank column's
+  // offset is its prefix minus the expert total.
+  const int total_c = block_exclusive_scan(tot, C, tmp);
+  const int total_e = kRank ? tot[E] : total_c;
+  const int total_r = total_c - total_e;
   if (cta == 0 && !kLL) {
     for (int e = tid; e <= E; e += NT) p.expert_off[e] = (e < E) ? tot[e] : total_e;
     if (kRank)
-      for (int r = tid; r <= R; r += NT) p.rank_off[r] = (r < R) ? tot[E + r] : total_r;
+      for (int r = tid; r <= R; r += NT) p.rank_off[r] = (r < R) ? tot[E + r] - total_e : total_r;
   }
   if (kLL) {
     // Chunks are source ranks here: (offset << 32) | count of expert e's rows from source `cta`.
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   }
   // Running counters: warp prefix + chunk prefix (+ global offset in normal mode).
   for (int col = w; col < C; col += W) {
-    if (lane < W) hist[lane * CP + col] += base[col] + (kLL ? 0 : tot[col]);
+    if (lane < W) hist[lane * CP + col] += base[col] + (kLL ? 0 : tot[col] - (col >= E ? total_e : 0));
   }
   __syncthreads();
 
