@@ -70,6 +70,8 @@ def parse():
                     help="low-latency workloads: combine in one launch, or send + receive hook")
     ap.add_argument("--mask-ranks", default="",
                     help="low-latency workloads: comma-separated ranks masked in the workspace (shrink mode)")
+    ap.add_argument("--fused-layout", action="store_true",
+                    help="normal workloads: layout and dispatch through one call (ep_layout_dispatch), timed as one phase")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
@@ -194,7 +196,8 @@ def fp8_flag_word(ep, cfg, scales: str) -> int:
 class NormalWorkload:
     """Layout, dispatch (per-rank + expert-major, BF16 or FP8), combine."""
 
-    def __init__(self, cfg, dev, inp, scales="fp32", align=1, bias=False, two_level=False, training=False):
+    def __init__(self, cfg, dev, inp, scales="fp32", align=1, bias=False, two_level=False, training=False,
+                 fused=False):
         import torch
         import combine_ep_get_dispatch_gb300 as ep
         self.ep, self.cfg = ep, cfg
@@ -235,7 +238,11 @@ class NormalWorkload:
             ep.ep_dispatch(lay0, self.x, False, None, None, ep._recv_struct(self.y, None, None))
         else:
             self.y = self.exp_x
-        self.phases = ["layout", "dispatch"] + (["combine_to_ranks", "combine_ranks"] if two_level else ["combine"])
+        # fused: layout and dispatch through one call (ep_layout_dispatch), the
+        # dispatch launched as the layout's programmatic dependent: one phase.
+        self.fused = fused
+        self.phases = (["layout+dispatch"] if fused else ["layout", "dispatch"]) + \
+            (["combine_to_ranks", "combine_ranks"] if two_level else ["combine"])
         self.training = training
         if training:
             # Backward: a gradient of the combined output flows back through
@@ -245,8 +252,10 @@ class NormalWorkload:
             self.grad_w = torch.empty((N, K), dtype=torch.float32, device=dev)
             self.grad_x = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
             self.phases += ["combine_backward", "dispatch_backward"]
-        self.dominant = "dispatch"
-        self.kernel_names = {"layout": "layout_kernel", "dispatch": f"dispatch_kernel<{'fp8' if cfg.fp8 else 'bf16'}>",
+        self.dominant = "layout+dispatch" if fused else "dispatch"
+        dk = f"dispatch_kernel<{'fp8' if cfg.fp8 else 'bf16'}>"
+        self.kernel_names = {"layout": "layout_kernel", "dispatch": dk,
+                             "layout+dispatch": f"layout_kernel + {dk} (programmatic dependent pair)",
                              "combine": "combine_kernel", "combine_to_ranks": "combine_to_ranks_kernel",
                              "combine_ranks": "combine_kernel"}
 
@@ -259,32 +268,34 @@ class NormalWorkload:
     def run(self, stream, x, idx_layout, w, ev=None, out=None):
         ep = self.ep
         out = self.out if out is None else out
-        if ev:
-            ev[0].record(stream)
-        ep.ep_get_dispatch_layout(idx_layout, self.ws, self.status, stream)
-        if ev:
-            ev[1].record(stream)
-        ep.ep_dispatch(idx_layout, x, self.flags, w, self.rb, self.eb, self.status, stream)
-        if ev:
-            ev[2].record(stream)
+        mark = iter(ev) if ev else None
+
+        def tick():
+            if mark is not None:
+                next(mark).record(stream)
+
+        tick()
+        if self.fused:
+            ep.ep_layout_dispatch(idx_layout, self.ws, x, self.flags, w, self.rb, self.eb, self.status, stream)
+            tick()
+        else:
+            ep.ep_get_dispatch_layout(idx_layout, self.ws, self.status, stream)
+            tick()
+            ep.ep_dispatch(idx_layout, x, self.flags, w, self.rb, self.eb, self.status, stream)
+            tick()
         if self.two_level:
             ep.ep_combine_to_ranks(idx_layout, self.y, w, self.rank_y, self.status, stream)
-            if ev:
-                ev[3].record(stream)
+            tick()
             ep.ep_combine_ranks(idx_layout, self.rank_y, out, self.status, stream, bias=self.bias)
-            if ev:
-                ev[4].record(stream)
+            tick()
             return
         ep.ep_combine(idx_layout, self.y, w, out, self.status, stream, bias=self.bias)
-        if ev:
-            ev[3].record(stream)
+        tick()
         if self.training:
             ep.ep_combine_backward(idx_layout, self.grad_out, self.y, w, self.grad_y, self.grad_w, self.status, stream)
-            if ev:
-                ev[4].record(stream)
+            tick()
             ep.ep_combine(idx_layout, self.grad_y, None, self.grad_x, self.status, stream)
-            if ev:
-                ev[5].record(stream)
+            tick()
 
     def rows(self):
         r = {"per_rank": int(self.lay.rank_offset[-1].item()),
@@ -308,12 +319,13 @@ class NormalWorkload:
         D_pad = rows.get("padded_expert_major", D_e)
         dispatch += (D_pad - D_e) * out_row                   # zeroed padding rows (aligned layouts)
         bias_b = N * 2 * H if self.bias is not None else 0
+        first = {"layout+dispatch": layout + dispatch} if self.fused else {"layout": layout, "dispatch": dispatch}
         if self.two_level:
-            return {"layout": layout, "dispatch": dispatch,
+            return {**first,
                     "combine_to_ranks": D_e * 2 * H + N * K * 12 + N * R * 4 + D_r * 2 * H,
                     "combine_ranks": D_r * 2 * H + N * R * 4 + N * 2 * H + bias_b}
         combine = D_e * 2 * H + N * K * 8 + N * 2 * H + bias_b  # rows + slots/weights read, out written
-        out = {"layout": layout, "dispatch": dispatch, "combine": combine}
+        out = {**first, "combine": combine}
         if self.training:
             # grad_out and the forward rows read, grad rows and grad_w written
             out["combine_backward"] = N * 2 * H + D_e * 2 * H * 2 + N * K * 12
@@ -432,7 +444,8 @@ def run_ours(args):
             ep.low_latency_update_mask_buffer(wl.ws, r, num_ranks=cfg.R)   # shrink mode: rank r is out
     else:
         wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales, align=args.expert_alignment,
-                            bias=args.combine_bias, two_level=args.combine == "two-level", training=args.training)
+                            bias=args.combine_bias, two_level=args.combine == "two-level", training=args.training,
+                            fused=args.fused_layout)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lay = wl.layout_for(wl.idx)
@@ -568,14 +581,14 @@ def run_ours(args):
                    "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
                                "combine": args.combine, "ll_combine": args.ll_combine,
                                "fp8_scales": args.fp8_scales, "training": args.training,
-                               "mask_ranks": args.mask_ranks},
+                               "mask_ranks": args.mask_ranks, "fused_layout": args.fused_layout},
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "rows": wl.rows()},
         "phases": phases,
         "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind},
-        "gpu_launches": (len(wl.phases) + (1 if cfg.mode == "ll" else 0)
+        "gpu_launches": (len(wl.phases) + (1 if cfg.mode == "ll" else 0) + (1 if getattr(wl, "fused", False) else 0)
                          + (1 if getattr(wl, "align", 1) > 1 else 0)) * args.steps,
         "clocks": sampler.summary(),
     }

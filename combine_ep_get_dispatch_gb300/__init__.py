@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         "ep_get_dispatch_layout": (I, [ctypes.POINTER(ep_layout_t), P, SZ, P, P]),
         "ep_dispatch": (I, [ctypes.POINTER(ep_layout_t), P, I, I, P, ctypes.POINTER(ep_recv_buffer_t),
                             ctypes.POINTER(ep_recv_buffer_t), P, P]),
+        "ep_layout_dispatch": (I, [ctypes.POINTER(ep_layout_t), P, SZ, P, I, I, P, ctypes.POINTER(ep_recv_buffer_t),
+                                   ctypes.POINTER(ep_recv_buffer_t), P, P]),
         "ep_combine": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P, P]),
         "ep_combine_to_ranks": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, I64, P, P]),
         "ep_combine_ranks": (I, [ctypes.POINTER(ep_layout_t), P, I64, I, P, P, P, P]),
@@ -251,6 +253,19 @@ def ep_dispatch(layout: Layout, x: torch.Tensor, fp8: int, topk_weights: Optiona
                              _p(status), _stream(stream)), "ep_dispatch")
 
 
+def ep_layout_dispatch(layout: Layout, workspace: torch.Tensor, x: torch.Tensor, fp8: int,
+                       topk_weights: Optional[torch.Tensor], rank_buf: Optional[ep_recv_buffer_t],
+                       expert_buf: Optional[ep_recv_buffer_t], status: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """ep_get_dispatch_layout then ep_dispatch in one call (the dispatch overlaps the layout)."""
+    c = layout.c_struct()
+    rb = ctypes.byref(rank_buf) if rank_buf is not None else None
+    eb = ctypes.byref(expert_buf) if expert_buf is not None else None
+    _check(lib().ep_layout_dispatch(ctypes.byref(c), _p(workspace), workspace.numel(), _p(x), x.shape[1],
+                                    int(fp8), _p(topk_weights), rb, eb, _p(status), _stream(stream)),
+           "ep_layout_dispatch")
+
+
 def ep_combine(layout: Layout, expert_y: torch.Tensor, topk_weights: torch.Tensor, out: torch.Tensor,
                status: Optional[torch.Tensor] = None, stream=None, bias: Optional[torch.Tensor] = None) -> None:
     c = layout.c_struct()
@@ -376,26 +391,12 @@ class DispatchResult:
     expert_src: Optional[torch.Tensor] = None    # [cap_e] int32 t*K + k
 
 
-def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tensor] = None,
-             use_fp8: bool = False, with_rank: bool = True, with_expert: bool = True,
-             exact: bool = False, status: Optional[torch.Tensor] = None, stream=None,
-             round_scale: bool = False, use_ue8m0: bool = False) -> DispatchResult:
-    """Scatter x [N, H] bf16 into per-rank and expert-major receive buffers.
-
-    exact=False sizes the buffers for the worst case (N*min(K,R) and N*K
-    rows), with no host synchronisation; exact=True reads the counts first
-    (one device->host copy) and sizes them exactly.
-    """
-    N, H = x.shape
+def _recv_buffers(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tensor], use_fp8: bool,
+                  use_ue8m0: bool, with_rank: bool, with_expert: bool, cap_r: int, cap_e: int):
+    """Receive buffers of a dispatch (capacities cap_r, cap_e rows) and their C structs."""
+    H = x.shape[1]
     K = layout.topk_idx.shape[1]
-    R = layout.num_ranks
     dev = x.device
-    if exact:
-        cap_r = int(layout.rank_offset[-1].item())
-        cap_e = int(layout.expert_offset[-1].item())
-    else:
-        A = max(1, layout.expert_alignment)
-        cap_r, cap_e = N * min(K, R), N * K + layout.num_experts * (A - 1)
     xdt = torch.uint8 if use_fp8 else torch.bfloat16
     sdt = torch.uint8 if use_ue8m0 else torch.float32
     S = H // 128
@@ -415,9 +416,62 @@ def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tenso
         res.expert_scales = torch.empty((cap_e, S), dtype=sdt, device=dev) if use_fp8 else None
         res.expert_src = torch.empty(cap_e, dtype=torch.int32, device=dev)
         eb = _recv_struct(res.expert_x, res.expert_scales, res.expert_src)
+    return res, rb, eb
+
+
+def _worst_case_caps(N: int, layout: Layout):
+    K = layout.topk_idx.shape[1]
+    A = max(1, layout.expert_alignment)
+    return N * min(K, layout.num_ranks), N * K + layout.num_experts * (A - 1)
+
+
+def dispatch(x: torch.Tensor, layout: Layout, topk_weights: Optional[torch.Tensor] = None,
+             use_fp8: bool = False, with_rank: bool = True, with_expert: bool = True,
+             exact: bool = False, status: Optional[torch.Tensor] = None, stream=None,
+             round_scale: bool = False, use_ue8m0: bool = False) -> DispatchResult:
+    """Scatter x [N, H] bf16 into per-rank and expert-major receive buffers.
+
+    exact=False sizes the buffers for the worst case (N*min(K,R) and N*K
+    rows), with no host synchronisation; exact=True reads the counts first
+    (one device->host copy) and sizes them exactly.
+    """
+    if exact:
+        cap_r = int(layout.rank_offset[-1].item())
+        cap_e = int(layout.expert_offset[-1].item())
+    else:
+        cap_r, cap_e = _worst_case_caps(x.shape[0], layout)
+    res, rb, eb = _recv_buffers(x, layout, topk_weights, use_fp8, use_ue8m0, with_rank, with_expert, cap_r, cap_e)
     tw = topk_weights.contiguous() if topk_weights is not None else None
     ep_dispatch(layout, x.contiguous(), fp8_flags(use_fp8, round_scale, use_ue8m0), tw, rb, eb, status, stream)
     return res
+
+
+def get_layout_and_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, num_experts: int, num_ranks: int,
+                            topk_weights: Optional[torch.Tensor] = None, use_fp8: bool = False,
+                            with_rank: bool = True, with_expert: bool = True,
+                            status: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            stream=None, expert_alignment: int = 1, round_scale: bool = False,
+                            use_ue8m0: bool = False):
+    """get_dispatch_layout and dispatch in one library call (ep_layout_dispatch).
+
+    Returns (layout, DispatchResult). The dispatch overlaps the layout on the
+    GPU; the receive buffers are sized for the worst case, since the counts
+    are not known before the call.
+    """
+    topk_idx = topk_idx.to(torch.int32).contiguous()
+    N, K = topk_idx.shape
+    layout = new_layout(topk_idx, num_experts, num_ranks, expert_alignment)
+    need = ep_layout_workspace_bytes(N, K, num_experts, num_ranks)
+    if need == 0:
+        raise EPError("get_layout_and_dispatch", EP_ERR_INVALID_ARG)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=topk_idx.device)
+    cap_r, cap_e = _worst_case_caps(N, layout)
+    res, rb, eb = _recv_buffers(x, layout, topk_weights, use_fp8, use_ue8m0, with_rank, with_expert, cap_r, cap_e)
+    tw = topk_weights.contiguous() if topk_weights is not None else None
+    ep_layout_dispatch(layout, workspace, x.contiguous(), fp8_flags(use_fp8, round_scale, use_ue8m0), tw, rb, eb,
+                       status, stream)
+    return layout, res
 
 
 def combine(expert_y: torch.Tensor, layout: Layout, topk_weights: torch.Tensor,

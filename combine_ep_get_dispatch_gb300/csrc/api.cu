@@ -123,8 +123,14 @@ size_t ep_layout_workspace_bytes(int N, int K, int E, int R) {
   return layout_ws(N, K, E, R).total;
 }
 
-int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status,
-                           void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks and parameters of a normal-mode layout into the handle L. Returns
+// EP_OK and fills p and G, or an error code (nothing is enqueued).
+int layout_setup(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status, LayoutParams& p,
+                 int& G) {
   if (!layout_ok(L)) return EP_ERR_INVALID_ARG;
   const int N = L->num_tokens, K = L->num_topk, E = L->num_experts, R = L->num_ranks;
   if (!L->num_tokens_per_rank || !L->num_tokens_per_expert || !L->rank_offset || !L->expert_offset)
@@ -134,11 +140,11 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
   const LayoutWs w = layout_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return EP_ERR_ALIGNMENT;
-  int G = layout_ctas_wanted(N, K);
+  G = layout_ctas_wanted(N, K);
   const int gmax = layout_max_ctas(E, R, true);
   if (gmax < 1) return EP_ERR_UNSUPPORTED;
   if (G > gmax) G = gmax;
-  LayoutParams p{};
+  p = LayoutParams{};
   p.idx = L->topk_idx;
   p.N = N; p.K = K; p.E = E; p.R = R; p.L = E / R;
   p.tokens_per_cta = (N + G - 1) / G;
@@ -154,18 +160,20 @@ int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspa
   p.ws_chunk = at<int32_t>(workspace, w.chunk);
   p.ws_barrier = at<unsigned>(workspace, w.barrier);
   p.status = status;
-  return cuda_rc(launch_layout(p, G, true, false, static_cast<cudaStream_t>(stream)));
+  return EP_OK;
 }
 
-int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, const float* topk_weights,
-                const ep_recv_buffer_t* rank_buf, const ep_recv_buffer_t* expert_buf, int32_t* status,
-                void* stream) {
+// Checks and parameters of a dispatch through the handle L. Returns EP_OK and
+// fills p (p.rank_x and p.exp_x both null: nothing to copy), or an error code.
+int dispatch_setup(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, const float* topk_weights,
+                   const ep_recv_buffer_t* rank_buf, const ep_recv_buffer_t* expert_buf, int32_t* status,
+                   DispatchParams& p) {
   if (!layout_ok(L) || !flags_ok(fp8_flags) || !hidden_ok(hidden, fp8_flags)) return EP_ERR_INVALID_ARG;
   const int use_fp8 = fp8_flags & EP_FP8;
   const int N = L->num_tokens, K = L->num_topk, E = L->num_experts, R = L->num_ranks;
   if (N > 0 && !x) return EP_ERR_INVALID_ARG;
   if (!aligned16(x)) return EP_ERR_ALIGNMENT;
-  DispatchParams p{};
+  p = DispatchParams{};
   p.x = static_cast<const uint16_t*>(x);
   p.N = N; p.K = K; p.H = hidden; p.E = E; p.R = R; p.L = E / R;
   p.idx = L->topk_idx;
@@ -198,23 +206,70 @@ int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, 
     p.exp_src = expert_buf->src_idx;
     p.exp_cap = expert_buf->capacity;
   }
+  return EP_OK;
+}
+
+// The dispatch launch (after_layout: as the programmatic dependent of the
+// layout launched just before by the same call), then, for an aligned layout,
+// the zero-fill of the expert-major padding rows.
+int dispatch_launch(const ep_layout_t* L, const DispatchParams& p, int fp8_flags, int32_t* status, cudaStream_t s,
+                    bool after_layout) {
   if (!p.rank_x && !p.exp_x) return EP_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int rc = cuda_rc(launch_dispatch(p, use_fp8 != 0, s));
+  const int use_fp8 = fp8_flags & EP_FP8;
+  const int rc = cuda_rc(launch_dispatch(p, use_fp8 != 0, s, after_layout));
   if (rc != EP_OK || !p.exp_x || L->expert_alignment <= 1) return rc;
-  // Aligned layout: zero the padding rows of the expert-major buffer.
   PadParams pp{};
   pp.expert_off = L->expert_offset;
   pp.per_expert = L->num_tokens_per_expert;
-  pp.E = E;
+  pp.E = L->num_experts;
   pp.x = p.exp_x;
-  pp.row_bytes = static_cast<int64_t>(hidden) * (use_fp8 ? 1 : 2);
+  pp.row_bytes = static_cast<int64_t>(p.H) * (use_fp8 ? 1 : 2);
   pp.scales = static_cast<uint8_t*>(p.exp_scales);
-  pp.scale_row_bytes = static_cast<int64_t>(hidden / 128) * ((fp8_flags & EP_FP8_UE8M0) ? 1 : 4);
+  pp.scale_row_bytes = static_cast<int64_t>(p.H / 128) * ((fp8_flags & EP_FP8_UE8M0) ? 1 : 4);
   pp.src = p.exp_src;
   pp.cap = p.exp_cap;
   pp.status = status;
   return cuda_rc(launch_pad_zero(pp, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status,
+                           void* stream) {
+  LayoutParams p;
+  int G = 0;
+  const int rc = layout_setup(L, workspace, workspace_bytes, status, p, G);
+  if (rc != EP_OK) return rc;
+  return cuda_rc(launch_layout(p, G, true, false, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, const float* topk_weights,
+                const ep_recv_buffer_t* rank_buf, const ep_recv_buffer_t* expert_buf, int32_t* status,
+                void* stream) {
+  DispatchParams p;
+  const int rc = dispatch_setup(L, x, hidden, fp8_flags, topk_weights, rank_buf, expert_buf, status, p);
+  if (rc != EP_OK) return rc;
+  return dispatch_launch(L, p, fp8_flags, status, static_cast<cudaStream_t>(stream), false);
+}
+
+int ep_layout_dispatch(const ep_layout_t* L, void* workspace, size_t workspace_bytes, const void* x, int hidden,
+                       int fp8_flags, const float* topk_weights, const ep_recv_buffer_t* rank_buf,
+                       const ep_recv_buffer_t* expert_buf, int32_t* status, void* stream) {
+  LayoutParams lp;
+  DispatchParams dp;
+  int G = 0;
+  // The dispatch checks first: they need no device, the layout's ask for its
+  // co-resident CTA limit.
+  int rc = dispatch_setup(L, x, hidden, fp8_flags, topk_weights, rank_buf, expert_buf, status, dp);
+  if (rc != EP_OK) return rc;
+  rc = layout_setup(L, workspace, workspace_bytes, status, lp, G);
+  if (rc != EP_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = cuda_rc(launch_layout(lp, G, true, false, s));
+  if (rc != EP_OK) return rc;
+  return dispatch_launch(L, dp, fp8_flags, status, s, true);
 }
 
 int ep_combine(const ep_layout_t* L, const void* expert_y, int64_t y_rows, int hidden,

@@ -239,6 +239,29 @@ int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags,
                 const ep_recv_buffer_t* expert_buf, int32_t* status, void* stream);
 
 /*
+ * Layout and dispatch in one call: the same work, arguments, results, status
+ * bits and error codes as ep_get_dispatch_layout(L, workspace,
+ * workspace_bytes, status, stream) followed by ep_dispatch(L, x, hidden,
+ * fp8_flags, topk_weights, rank_buf, expert_buf, status, stream). Every
+ * argument of both is checked before anything is enqueued.
+ * (The two steps of the DeepEP V1 guide, section 5.1: get_dispatch_layout,
+ * then dispatch with its counts and mask.)
+ *
+ * The dispatch is launched as the programmatic dependent of the layout
+ * (programmatic dependent launch): its blocks start while the layout runs,
+ * bring in (and quantise) their token rows, and wait in-kernel for the layout
+ * to complete before they read any slot. So x, topk_idx and topk_weights must
+ * be ready when the call is enqueued, as for any stream-ordered call; nothing
+ * else changes for the caller.
+ * Receive buffers must exist before the call: size them for the worst case
+ * (see ep_recv_buffer_t), since the counts are not known on the host.
+ */
+int ep_layout_dispatch(const ep_layout_t* L, void* workspace, size_t workspace_bytes,
+                       const void* x, int hidden, int fp8_flags, const float* topk_weights,
+                       const ep_recv_buffer_t* rank_buf, const ep_recv_buffer_t* expert_buf,
+                       int32_t* status, void* stream);
+
+/*
  * Combine: gather the expert outputs back along the dispatch path and take
  * the router-weighted sum: out[t] = bf16( sum over k = 0..K-1 with
  * expert_slot[t, k] >= 0 of w[t, k] * y[expert_slot[t, k]] ), accumulated in

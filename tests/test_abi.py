@@ -76,6 +76,18 @@ def test_host_validation_rejects_before_cuda(L):
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 60, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 64, 1, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_dispatch(ctypes.byref(lay), P(16), 32768, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
+    # layout + dispatch in one call: the dispatch arguments are checked first, then the layout's
+    LD = L.ep_layout_dispatch
+    assert LD(None, P(256), 1 << 20, P(16), 64, 0, None, None, None, None, None) == ep.EP_ERR_INVALID_ARG
+    assert LD(ctypes.byref(lay), P(256), 1 << 20, P(18), 64, 0, None, None, None, None, None) \
+        == ep.EP_ERR_ALIGNMENT
+    assert LD(ctypes.byref(lay), P(256), 1 << 20, P(16), 60, 0, None, None, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG
+    assert LD(ctypes.byref(lay), P(256), 1 << 20, P(16), 128, ep.EP_FP8_UE8M0, None, None, None, None, None) \
+        == ep.EP_ERR_INVALID_ARG
+    assert LD(ctypes.byref(lay), P(256), 16, P(16), 64, 0, None, None, None, None, None) == ep.EP_ERR_WORKSPACE
+    assert LD(ctypes.byref(lay), P(264), 1 << 20, P(16), 64, 0, None, None, None, None, None) \
+        == ep.EP_ERR_ALIGNMENT
     # combine: misaligned output
     assert L.ep_combine(ctypes.byref(lay), P(16), 10, 64, P(16), None, P(24), None, None) == ep.EP_ERR_ALIGNMENT
     assert L.ep_combine(ctypes.byref(lay), P(16), 10, 64, P(16), P(40), P(32), None, None) == ep.EP_ERR_ALIGNMENT

@@ -141,6 +141,58 @@ def test_normal_path_in_a_cuda_graph():
     assert status_value(st) == 0
 
 
+def test_layout_dispatch_pair_in_a_cuda_graph():
+    """ep_layout_dispatch (a programmatic-dependent pair of launches) + combine
+    captured once, replayed on two batches."""
+    cfg = ei.CONFIGS[5].scaled(N=700, H=1024)
+    N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
+    x = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    lay = ep.new_layout(idx, E, R)
+    ws = torch.zeros(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device="cuda")
+    rx = torch.empty((N * min(K, R), H), dtype=torch.uint8, device="cuda")
+    rs = torch.empty((N * min(K, R), H // 128), dtype=torch.float32, device="cuda")
+    rsrc = torch.empty(N * min(K, R), dtype=torch.int32, device="cuda")
+    ex = torch.empty((N * K, H), dtype=torch.uint8, device="cuda")
+    es = torch.empty((N * K, H // 128), dtype=torch.float32, device="cuda")
+    y = torch.empty((N * K, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+    st = _status()
+
+    def step():
+        ep.ep_layout_dispatch(lay, ws, x, True, w, ep._recv_struct(rx, rs, rsrc), ep._recv_struct(ex, es, None), st)
+        ep.ep_combine(lay, y, w, out, st)
+
+    y.copy_(to_dev_bf16(_expert_outputs((N * K, H), 7)))
+    d0 = ei.make_inputs(cfg, seed=50)
+    x.copy_(to_dev_bf16(d0["x"])); idx.copy_(to_dev(d0["topk_idx"])); w.copy_(to_dev(d0["topk_weights"]))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (51, 52):
+        d = ei.make_inputs(cfg, seed=seed)
+        x.copy_(to_dev_bf16(d["x"])); idx.copy_(to_dev(d["topk_idx"])); w.copy_(to_dev(d["topk_weights"]))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.dispatch(d["x"], d["topk_idx"], d["topk_weights"], E, R, True)
+        D_e, D_r = ref["exp_x"].shape[0], ref["rank_x"].shape[0]
+        assert np.array_equal(u8(ex[:D_e]), ref["exp_x"])
+        assert np.array_equal(es[:D_e].cpu().numpy(), ref["exp_scales"])
+        assert np.array_equal(u8(rx[:D_r]), ref["rank_x"])
+        assert np.array_equal(rs[:D_r].cpu().numpy(), ref["rank_scales"])
+        assert np.array_equal(rsrc[:D_r].cpu().numpy(), ref["rank_src"])
+        ref_out, _ = oracle.combine(u16(y), ref["layout"]["expert_slot"], d["topk_weights"])
+        assert np.array_equal(u16(out), ref_out)
+    assert status_value(st) == 0
+
+
 @pytest.mark.parametrize("round_scale,ue8m0", [(True, False), (False, True)])
 def test_dispatch_power_of_two_and_ue8m0_scales(round_scale, ue8m0):
     cfg = ei.CONFIGS[5].scaled(N=700, H=4096)

@@ -186,6 +186,64 @@ def test_dispatch_expert_only_and_rank_only():
     assert np.array_equal(u16(res.rank_x), ref["rank_x"]) and res.rank_x.shape[0] == D_r
 
 
+@pytest.mark.parametrize("c,N,H,use_fp8", [(3, 1000, 7168, True), (4, 777, 7168, False), (5, 1500, 4096, True),
+                                           (4, 333, 8, False), (3, 257, 128, False), (5, 64, 1024, True)])
+def test_layout_and_dispatch_in_one_call(c, N, H, use_fp8):
+    """ep_layout_dispatch (the dispatch launched as the layout's programmatic
+    dependent) gives the oracle's layout and receive rows."""
+    cfg = ei.CONFIGS[c].scaled(N=N, H=H)
+    d = ei.make_inputs(cfg, seed=c + 20)
+    st = _status()
+    lay, res = ep.get_layout_and_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), cfg.E, cfg.R,
+                                          to_dev(d["topk_weights"]), use_fp8=use_fp8, status=st)
+    _layout_equal(lay, oracle.layout(d["topk_idx"], cfg.E, cfg.R))
+    ref = oracle.dispatch(d["x"], d["topk_idx"], d["topk_weights"], cfg.E, cfg.R, use_fp8)
+    _check_dispatch(res, ref, use_fp8, cfg.K)
+    assert status_value(st) == 0
+
+
+def _same_dispatch(lay1, r1, lay2, r2):
+    for k in LAYOUT_KEYS:
+        assert torch.equal(getattr(lay1, k), getattr(lay2, k)), k
+    D_e, D_r = int(lay1.expert_offset[-1].item()), int(lay1.rank_offset[-1].item())
+    for name, D in (("expert_x", D_e), ("expert_scales", D_e), ("expert_src", D_e), ("rank_x", D_r),
+                    ("rank_scales", D_r), ("rank_src", D_r), ("rank_topk_idx", D_r), ("rank_topk_weights", D_r)):
+        a, b = getattr(r1, name), getattr(r2, name)
+        assert (a is None) == (b is None), name
+        if a is not None:
+            assert torch.equal(a[:D], b[:D]), name
+
+
+@pytest.mark.parametrize("c", [3, 4, 5])
+def test_layout_and_dispatch_full_size_matches_two_calls(c):
+    """On the full workloads the one-call path writes exactly what
+    ep_get_dispatch_layout + ep_dispatch write (checked against the oracle above)."""
+    cfg = ei.CONFIGS[c]
+    d = ei.make_inputs(cfg, seed=0)
+    x, idx, w = to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
+    st = _status()
+    lay1 = ep.get_dispatch_layout(idx, cfg.E, cfg.R, status=st)
+    r1 = ep.dispatch(x, lay1, w, use_fp8=cfg.fp8, status=st)
+    lay2, r2 = ep.get_layout_and_dispatch(x, idx, cfg.E, cfg.R, w, use_fp8=cfg.fp8, status=st)
+    _same_dispatch(lay1, r1, lay2, r2)
+    assert status_value(st) == 0
+    del r1, r2
+    torch.cuda.empty_cache()
+
+
+def test_layout_and_dispatch_aligned_with_padding():
+    """Expert segments padded to 128 rows: padding rows are zero-filled by the one-call path too."""
+    cfg = ei.CONFIGS[3].scaled(N=600, H=1024)
+    d = ei.make_inputs(cfg, seed=31)
+    x, idx, w = to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
+    st = _status()
+    lay1 = ep.get_dispatch_layout(idx, cfg.E, cfg.R, status=st, expert_alignment=128)
+    r1 = ep.dispatch(x, lay1, w, use_fp8=True, status=st)
+    lay2, r2 = ep.get_layout_and_dispatch(x, idx, cfg.E, cfg.R, w, use_fp8=True, status=st, expert_alignment=128)
+    _same_dispatch(lay1, r1, lay2, r2)
+    assert status_value(st) == 0
+
+
 def test_dispatch_capacity_overflow_flagged():
     cfg = ei.CONFIGS[4].scaled(N=400, H=256)
     d = ei.make_inputs(cfg, seed=4)
