@@ -423,6 +423,39 @@ class LLWorkload:
         return {"send": send, "recv": recv, "combine": combine}
 
 
+def workload_config(cfg, args, world, rows):
+    """The line's `config`: the workload, its variant flags and its row counts (both arms print the same)."""
+    return {"workload": cfg.name, "tokens": cfg.N, "hidden": cfg.H, "experts": cfg.E, "topk": cfg.K,
+            "ranks": cfg.R, "max_tokens_per_rank": cfg.T,
+            "dispatch_dtype": (f"fp8_e4m3 + {args.fp8_scales} scales / 128 ch" if cfg.fp8 else "bf16"),
+            "combine_dtype": "bf16 (fp32 accumulation)",
+            "l2": "flushed between steps (256 MiB write)",
+            "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
+                        "combine": args.combine, "ll_combine": args.ll_combine,
+                        "fp8_scales": args.fp8_scales, "training": args.training,
+                        "mask_ranks": args.mask_ranks, "fused_layout": args.fused_layout},
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "rows": rows}
+
+
+def oracle_rows(cfg, args):
+    """Row counts of the full workload from the oracle's layout (the reference arm's copy of wl.rows())."""
+    import oracle
+    idx = ei.make_inputs(cfg, seed=0, with_x=False)["topk_idx"]
+    if cfg.mode == "ll":
+        mask = np.zeros(cfg.R, np.int32)
+        for r in (int(v) for v in args.mask_ranks.split(",") if v):
+            mask[r] = 1
+        if mask.any():
+            idx = oracle.ll_mask_routing(idx, cfg.E, cfg.R, mask)
+        return {"received": int(oracle.layout(idx, cfg.E, cfg.R)["num_tokens_per_expert"].sum())}
+    lay = oracle.layout(idx, cfg.E, cfg.R, max(1, args.expert_alignment))
+    r = {"per_rank": int(lay["rank_offset"][-1]), "expert_major": int(lay["num_tokens_per_expert"].sum())}
+    if args.expert_alignment > 1:
+        r["padded_expert_major"] = int(lay["expert_offset"][-1])
+    return r
+
+
 def run_ours(args):
     import torch
     import combine_ep_get_dispatch_gb300 as ep
@@ -573,17 +606,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded: x ~ N(0,1) BF16, router logits N(0,1) softmax top-k renormalised; "
                 "see epinputs for the grouped and Zipf recipes)",
-        "config": {"workload": cfg.name, "tokens": N, "hidden": cfg.H, "experts": cfg.E, "topk": cfg.K,
-                   "ranks": cfg.R, "max_tokens_per_rank": cfg.T,
-                   "dispatch_dtype": (f"fp8_e4m3 + {args.fp8_scales} scales / 128 ch" if cfg.fp8 else "bf16"),
-                   "combine_dtype": "bf16 (fp32 accumulation)",
-                   "l2": "flushed between steps (256 MiB write)",
-                   "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
-                               "combine": args.combine, "ll_combine": args.ll_combine,
-                               "fp8_scales": args.fp8_scales, "training": args.training,
-                               "mask_ranks": args.mask_ranks, "fused_layout": args.fused_layout},
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "rows": wl.rows()},
+        "config": workload_config(cfg, args, world, wl.rows()),
         "phases": phases,
         "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -662,9 +685,10 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": cfg.name, "tokens_per_step_sample": n_tok},
+            "data": "synthetic", "config": workload_config(cfg, args, world, oracle_rows(cfg, args)),
             "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s", "kind": "oracle", "cores": 1,
-                             "sample": f"{n_tok} tokens of {cfg.name} per step"},
+                             "sample": f"{n_tok} tokens of {cfg.name} per step (the whole step: layout, "
+                                       f"dispatch and combine on those tokens)"},
             "e2e": {"value": round(v, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
