@@ -183,7 +183,11 @@ size_t ep_layout_workspace_bytes(int num_tokens, int num_topk, int num_experts, 
  *              before its first use (or a previous call on it timed out).
  *              After either of the last two the outputs are invalid and the
  *              workspace must be zero-filled again.
- * Runs as one cooperative launch.
+ * Runs as one cooperative launch. The kernel releases programmatic dependents
+ * at its start: a kernel the caller launches right after it with programmatic
+ * stream serialization may begin at once and must wait on the grid dependency
+ * (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads any of
+ * the layout's outputs. Kernels launched without that attribute are unaffected.
  */
 int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes,
                            int32_t* status, void* stream);
