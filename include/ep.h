@@ -380,8 +380,11 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *   status       EP_ST_BAD_INDEX, EP_ST_TIMEOUT and EP_ST_WORKSPACE as for
  *                the layout
  * Slots of ranks masked in the workspace (shrink mode, ep_ll_update_mask)
- * are dropped. Enqueues two launches. The rows are in place when the stream reaches the
- * end of this call; the counts are published by ep_ll_dispatch_recv.
+ * are dropped. Enqueues two launches: the routing layout, then the row
+ * copies as its programmatic dependent (they load and quantise their rows
+ * while the layout runs, and wait for it in-kernel before reading a slot).
+ * The rows are in place when the stream reaches the end of this call; the
+ * counts are published by ep_ll_dispatch_recv.
  */
 int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, int num_topk,
                         int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
