@@ -231,6 +231,32 @@ def test_layout_and_dispatch_full_size_matches_two_calls(c):
     torch.cuda.empty_cache()
 
 
+def test_layout_and_dispatch_empty_masked_and_bad_indices():
+    """The one-call path on an empty batch, and on a routing with masked slots and
+    out-of-range indices: the same rows and status bits as the two calls."""
+    H = 256
+    x0 = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    st = _status()
+    lay, res = ep.get_layout_and_dispatch(x0, torch.empty((0, 4), dtype=torch.int32, device="cuda"), 32, 4,
+                                          torch.empty((0, 4), dtype=torch.float32, device="cuda"), status=st)
+    assert lay.expert_offset.cpu().numpy().tolist() == [0] * 33
+    assert status_value(st) == 0
+    idx = _rand_idx(500, 4, 32, seed=5)
+    idx[::7, 1] = 32
+    idx[::11, 2] = -5
+    idx[::13, 3] = -1
+    d = ei.make_inputs(ei.CONFIGS[4].scaled(N=500, H=H, K=4, E=32, R=4), seed=6)
+    x, w = to_dev_bf16(d["x"]), to_dev(d["topk_weights"])
+    for fp8 in (False, True):
+        st1, st2 = _status(), _status()
+        lay1 = ep.get_dispatch_layout(to_dev(idx), 32, 4, status=st1)
+        r1 = ep.dispatch(x, lay1, w, use_fp8=fp8, status=st1)
+        lay2, r2 = ep.get_layout_and_dispatch(x, to_dev(idx), 32, 4, w, use_fp8=fp8, status=st2)
+        _same_dispatch(lay1, r1, lay2, r2)
+        assert status_value(st1) == status_value(st2) == ep.EP_ST_BAD_INDEX
+        _layout_equal(lay2, oracle.layout(idx, 32, 4))
+
+
 def test_layout_and_dispatch_aligned_with_padding():
     """Expert segments padded to 128 rows: padding rows are zero-filled by the one-call path too."""
     cfg = ei.CONFIGS[3].scaled(N=600, H=1024)
