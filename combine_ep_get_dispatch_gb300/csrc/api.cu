@@ -12,6 +12,8 @@ using namespace ep;
 constexpr int kVersion = 100;  // 0.1.0
 constexpr int64_t kEntriesPerCta = 1024;  // (token, slot) entries per layout CTA (measured)
 constexpr int kMaxLayoutCtas = 256;
+// Low-latency batches up to this many (token, slot) entries take the one-CTA layout.
+constexpr int64_t kLLOneCtaMaxEntries = 4096;
 
 inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -392,10 +394,20 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   if (gmax < 1 || R > gmax) return EP_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  // A small batch runs the layout as one CTA with a group of g warps per
+  // source rank (no grid barrier, no exchange of chunk counts through
+  // memory); each source rank's entries must split evenly over its g warps
+  // in whole multiples of 32.
+  const int ns = N / R;
+  int g = R <= 32 ? 32 / R : 0;
+  while (g > 0 && (ns * K) % (32 * g) != 0) --g;
+  const bool one_cta = N > 0 && g > 0 && static_cast<int64_t>(N) * K <= kLLOneCtaMaxEntries;
   LayoutParams lp{};
   lp.idx = topk_idx;
   lp.N = N; lp.K = K; lp.E = E; lp.R = R; lp.L = E / R;
-  lp.tokens_per_cta = (N / R > 0) ? N / R : 1;
+  lp.tokens_per_cta = one_cta ? N : (ns > 0 ? ns : 1);
+  lp.ll_src_entries = one_cta ? ns * K : 0;
+  lp.ll_src_warps = one_cta ? g : 0;
   lp.per_expert = at<int32_t>(workspace, w.count);
   lp.expert_slot = at<int32_t>(workspace, w.slot);
   lp.ll_cap = static_cast<int64_t>(R) * T;
@@ -406,7 +418,7 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   lp.ws_barrier = at<unsigned>(workspace, w.barrier);
   lp.rank_mask = at<int32_t>(workspace, w.mask);
   lp.status = status;
-  rc = cuda_rc(launch_layout(lp, R, false, true, s));
+  rc = cuda_rc(launch_layout(lp, one_cta ? 1 : R, false, true, s));
   if (rc != EP_OK) return rc;
 
   DispatchParams dp{};

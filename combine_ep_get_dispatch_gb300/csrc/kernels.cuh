@@ -36,6 +36,9 @@ struct LayoutParams {
   LLHeader* ll_hdr;
   LLHeader hdr_value;
   const int32_t* rank_mask;  // low-latency shrink mode: [R], non-zero = masked (or null)
+  int ll_src_entries;        // > 0: one-CTA low-latency form: source rank s holds entries
+                             // [s * ll_src_entries, (s + 1) * ll_src_entries), on warps
+  int ll_src_warps;          // [s * ll_src_warps, (s + 1) * ll_src_warps) (R * ll_src_warps <= 32)
   // scratch
   int32_t* ws_chunk;   // [G, C]
   unsigned* ws_barrier;

@@ -25,6 +25,11 @@
 // No atomics decide an order: slots follow (token, slot) order by
 // construction. The kernel is bound by instruction latency, not memory: the
 // traffic is a few hundred KB of int32.
+// Low latency: chunks are source ranks. A small batch instead runs as one CTA
+// in which a group of g warps holds each source rank's entries: the scan
+// across warps then gives the prefix over source ranks, and no grid barrier
+// or exchange through memory is needed (nor with a single chunk in normal
+// mode).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -119,7 +124,8 @@ __device__ __forceinline__ int entry_code_global(const LayoutParams& p, int64_t 
 }
 
 // Low-latency shrink mode: an entry is dropped (as if its index were -1) when
-// its source rank (the CTA's chunk) or the rank holding its expert is masked.
+// its source rank (the CTA's chunk, or its warp range in the one-CTA form) or
+// the rank holding its expert is masked.
 template <bool kLL>
 __device__ __forceinline__ bool ll_drop(const LayoutParams& p, int code, bool src_masked) {
   if (!kLL || code < 0 || !p.rank_mask) return false;
@@ -158,9 +164,15 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   bool bad = false;
   // The barrier's generation, read before any block can have arrived.
   const unsigned gen0 = (G > 1 && tid == 0) ? barrier_generation(p.ws_barrier) : 0u;
-  // Low-latency shrink mode: a masked source rank sends nothing (this CTA's
-  // chunk is that rank's tokens).
-  const bool src_masked = kLL && p.rank_mask && __ldg(p.rank_mask + cta) != 0;
+  // Low-latency shrink mode: a masked source rank sends nothing. An entry's
+  // source rank is this CTA's chunk or, in the one-CTA form (where source
+  // ranks are warp groups), the warp group that holds entry li.
+  const bool warp_src = kLL && p.ll_src_entries > 0;
+  const bool cta_src_masked = kLL && p.rank_mask && !warp_src && __ldg(p.rank_mask + cta) != 0;
+  auto src_masked = [&](int li) -> bool {
+    if (!kLL || !p.rank_mask) return false;
+    return warp_src ? __ldg(p.rank_mask + li / p.ll_src_entries) != 0 : cta_src_masked;
+  };
   for (int i = tid; i < W * CP; i += NT) hist[i] = 0;
   if (kStaged) {
     // One coalesced pass over the chunk's indices; each entry's rank is
@@ -187,7 +199,7 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
         }
         if (first) code |= kFirstBit;
       }
-      scode[li] = ll_drop<kLL>(p, code, src_masked) ? -1 : code;
+      scode[li] = ll_drop<kLL>(p, code, code >= 0 && src_masked(li)) ? -1 : code;
     }
   }
   __syncthreads();
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   // Pass 1: per-warp counts (shared-memory atomics: counting needs no order).
   for (int li = wa0 + lane; li < wa1; li += 32) {
     int code = kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad);
-    if (!kStaged && ll_drop<kLL>(p, code, src_masked)) code = -1;
+    if (!kStaged && ll_drop<kLL>(p, code, code >= 0 && src_masked(li))) code = -1;
     if (code >= 0) {
       atomicAdd(&my[code_e(code)], 1);
       if (kRank && (code & kFirstBit)) atomicAdd(&my[E + code_r(code)], 1);
@@ -230,10 +242,20 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     for (int j = 0; j < kScanCols; ++j) {
       const int col = c0 + j * W;
       if (col >= C) break;
+      if (warp_src && col < E) {
+        // One-CTA low-latency form: warps [s*g, (s+1)*g) hold source rank s,
+        // so its range of expert col is (prefix before its first warp, count
+        // up to the end of its last warp).
+        const int g = p.ll_src_warps;
+        const int last = __shfl_sync(0xffffffffu, incl[j], min(lane + g - 1, 31));
+        const int pre = incl[j] - v[j];
+        if (lane < W && lane % g == 0)
+          p.ll_range[static_cast<int64_t>(col) * R + lane / g] = (static_cast<int64_t>(pre) << 32) | (last - pre);
+      }
       if (lane < W) hist[lane * CP + col] = incl[j] - v[j];
       if (lane == 31) {
         own[col] = incl[j];
-        p.ws_chunk[static_cast<int64_t>(cta) * C + col] = incl[j];
+        if (G > 1) p.ws_chunk[static_cast<int64_t>(cta) * C + col] = incl[j];
       }
     }
   }
@@ -254,9 +276,10 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   // Prefix over earlier chunks and totals over all chunks. P threads share a
   // column (four columns when C % 4 == 0: 16-byte loads), each summing every
   // P-th chunk with all of its loads in flight at once.
+  // One CTA: no other chunks, the totals are its own counts.
   const int CV = (C % 4 == 0) ? C / 4 : 0;   // 16-byte column groups
   const int P = CV ? max(1, min(NT / CV, G)) : max(1, min(NT / C, G));
-  if (CV) {
+  if (G > 1 && CV) {
     const int4* chunk4 = reinterpret_cast<const int4*>(p.ws_chunk);
     for (int j = tid; j < P * CV; j += NT) {
       const int cv = j % CV, pp = j / CV;
@@ -281,7 +304,7 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
       part[PS + pp * C + col + 2] = total.z; part[PS + pp * C + col + 3] = total.w;
     }
   }
-  for (int j = tid; !CV && j < P * C; j += NT) {
+  for (int j = tid; G > 1 && !CV && j < P * C; j += NT) {
     const int col = j % C, pp = j / C;
     int pre = 0, total = 0, c = pp;
     for (; c + 7 * P < G; c += 8 * P) {
@@ -302,12 +325,15 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     part[j] = pre;  // j < P * C <= PS
     part[PS + j] = total;
   }
-  __syncthreads();
+  if (G > 1) __syncthreads();
   for (int col = tid; col < C; col += NT) {
-    int pre = 0, total = 0;
-    for (int pp = 0; pp < P; ++pp) {
-      pre += part[pp * C + col];
-      total += part[PS + pp * C + col];
+    int pre = 0, total = own[col];
+    if (G > 1) {
+      total = 0;
+      for (int pp = 0; pp < P; ++pp) {
+        pre += part[pp * C + col];
+        total += part[PS + pp * C + col];
+      }
     }
     base[col] = pre;
     tot[col] = total;
@@ -333,8 +359,9 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
       for (int r = tid; r <= R; r += NT) p.rank_off[r] = (r < R) ? tot[E + r] - total_e : total_r;
   }
   if (kLL) {
-    // Chunks are source ranks here: (offset << 32) | count of expert e's rows from source `cta`.
-    for (int e = tid; e < E; e += NT)
+    // Chunks are source ranks here: (offset << 32) | count of expert e's rows
+    // from source `cta` (the one-CTA form wrote its ranges in the column scan).
+    for (int e = tid; !warp_src && e < E; e += NT)
       p.ll_range[static_cast<int64_t>(e) * R + cta] =
           (static_cast<int64_t>(base[e]) << 32) | static_cast<int64_t>(own[e]);
     if (cta == 0 && tid == 0) *p.ll_hdr = p.hdr_value;
@@ -351,7 +378,7 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     const int li = b + lane;
     const bool in = li < wa1;
     int code = in ? (kStaged ? scode[li] : entry_code_global<kRank>(p, a0 + li, bad2)) : -1;
-    if (!kStaged && ll_drop<kLL>(p, code, src_masked)) code = -1;
+    if (!kStaged && ll_drop<kLL>(p, code, code >= 0 && src_masked(li))) code = -1;
     const bool valid = code >= 0;
     const int e = code_e(code);
     const unsigned pe = warp_peers(e, valid, p.bits_E);
@@ -454,7 +481,8 @@ int layout_max_ctas(int E, int R, bool with_rank) {
 cudaError_t launch_layout(const LayoutParams& p, int G, bool with_rank, bool ll, cudaStream_t s) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorNoDevice;
-  const int threads = layout_threads(p.E, p.R, with_rank);
+  // The one-CTA low-latency form runs ll_src_warps warps per source rank.
+  const int threads = p.ll_src_entries > 0 ? p.R * p.ll_src_warps * 32 : layout_threads(p.E, p.R, with_rank);
   const size_t entries = static_cast<size_t>(p.tokens_per_cta) * p.K;
   bool staged = entries <= kMaxStagedEntries;
   size_t smem = layout_smem(p.E, p.R, with_rank, threads, staged ? entries : 0);
