@@ -193,6 +193,69 @@ def test_layout_dispatch_pair_in_a_cuda_graph():
     assert status_value(st) == 0
 
 
+def test_overlapped_launches_back_to_back():
+    """Ten low-latency steps and ten one-call layout + dispatch + combine steps
+    enqueued back to back on one stream (new inputs and outputs each step, no
+    host synchronisation between them): every step matches the oracle. Each
+    step's layout starts behind the previous step's combine, and its dispatch
+    starts early behind the layout (programmatic dependent launch)."""
+    steps = 10
+    st = _status()
+    # low latency
+    cfg = ei.CONFIGS[1].scaled(H=1024)
+    N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
+    ins = [ei.make_inputs(cfg, seed=70 + i) for i in range(steps)]
+    xs = [to_dev_bf16(d["x"]) for d in ins]
+    ids = [to_dev(d["topk_idx"]) for d in ins]
+    ws_ = [to_dev(d["topk_weights"]) for d in ins]
+    ws = torch.zeros(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device="cuda")
+    recv = [torch.empty((E, R * T, H), dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    src = torch.empty((E, R * T), dtype=torch.int32, device="cuda")
+    cnt = [torch.empty(E, dtype=torch.int32, device="cuda") for _ in range(steps)]
+    outs = [torch.empty((N, H), dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+    for i in range(steps):
+        ep.ep_ll_dispatch_send(xs[i], ids[i], H, E, R, T, False, recv[i], None, src, ws, st)
+        ep.ep_ll_dispatch_recv(ws, N, K, E, R, T, cnt[i], None, st)
+        ep.ep_ll_combine(recv[i], ws_[i], ws, N, K, H, E, R, T, outs[i], st)
+    torch.cuda.synchronize()
+    for i, d in enumerate(ins):
+        ref = oracle.ll_dispatch(d["x"], d["topk_idx"], E, R, T, False)
+        c = cnt[i].cpu().numpy()
+        assert np.array_equal(c, ref["recv_count"])
+        got = u16(recv[i])
+        for e in range(E):
+            assert np.array_equal(got[e, :c[e]], ref["recv_x"][e, :c[e]])
+        ref_out, _ = oracle.ll_combine(ref["recv_x"], ref["slot_map"], d["topk_weights"])
+        assert np.array_equal(u16(outs[i]), ref_out)
+    # normal mode, layout + FP8 dispatch in one call, then combine of the BF16 rows
+    cfg = ei.CONFIGS[3].scaled(N=300, H=512)
+    N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
+    ins = [ei.make_inputs(cfg, seed=80 + i) for i in range(steps)]
+    ws = torch.zeros(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device="cuda")
+    y = torch.empty((N * K, H), dtype=torch.bfloat16, device="cuda")
+    y.copy_(to_dev_bf16(_expert_outputs((N * K, H), 9)))
+    res = []
+    for d in ins:
+        idx = to_dev(d["topk_idx"])
+        lay = ep.new_layout(idx, E, R)
+        ex = torch.empty((N * K, H), dtype=torch.uint8, device="cuda")
+        es = torch.empty((N * K, H // 128), dtype=torch.float32, device="cuda")
+        out = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+        ep.ep_layout_dispatch(lay, ws, to_dev_bf16(d["x"]), True, to_dev(d["topk_weights"]), None,
+                              ep._recv_struct(ex, es, None), st)
+        ep.ep_combine(lay, y, to_dev(d["topk_weights"]), out, st)
+        res.append((lay, ex, es, out))
+    torch.cuda.synchronize()
+    for d, (lay, ex, es, out) in zip(ins, res):
+        ref = oracle.dispatch(d["x"], d["topk_idx"], d["topk_weights"], E, R, True, with_rank=False)
+        D_e = ref["exp_x"].shape[0]
+        assert np.array_equal(u8(ex[:D_e]), ref["exp_x"])
+        assert np.array_equal(es[:D_e].cpu().numpy(), ref["exp_scales"])
+        ref_out, _ = oracle.combine(u16(y), ref["layout"]["expert_slot"], d["topk_weights"])
+        assert np.array_equal(u16(out), ref_out)
+    assert status_value(st) == 0
+
+
 @pytest.mark.parametrize("round_scale,ue8m0", [(True, False), (False, True)])
 def test_dispatch_power_of_two_and_ue8m0_scales(round_scale, ue8m0):
     cfg = ei.CONFIGS[5].scaled(N=700, H=4096)
