@@ -2,8 +2,9 @@
 //
 // Inline PTX for the Blackwell data-movement primitives used on the hot path:
 // the bulk (non-tensor) TMA copies global -> shared (completing on an
-// mbarrier) and shared -> global (bulk groups), the async-proxy fence, and
-// the acquire loads of the bounded grid-wide barrier.
+// mbarrier) and shared -> global (bulk groups), the async-proxy fence, the
+// streaming row load, the programmatic-dependent-launch controls, and the
+// acquire loads of the bounded grid-wide barrier.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -93,12 +94,6 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-// Wait until at most N of this thread's bulk groups are incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -106,14 +101,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---- loads ----------------------------------------------------------------
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // A 16-byte load of data read exactly once: no L1 allocation, and first in
 // line for eviction from L2 (an evict-first access policy), so the stream of
 // rows does not push out data that is still wanted.
@@ -126,11 +113,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
       : "l"(p));
   return v;
-}
-
-__device__ __forceinline__ void st_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {

@@ -173,6 +173,28 @@ def test_dispatch_parity(c, N, H, use_fp8):
     assert status_value(st) == 0
 
 
+@pytest.mark.parametrize("use_fp8", [False, True])
+def test_maximum_sizes(use_fp8):
+    """The largest shapes the ABI accepts: hidden 16384, top-32, 1024 experts
+    on 1024 ranks (one expert each): layout, both receive buffers and combine
+    against the oracle."""
+    N, H, K, E, R = 70, ep.EP_MAX_HIDDEN, ep.EP_MAX_TOPK, ep.EP_MAX_EXPERTS, ep.EP_MAX_EXPERTS
+    idx = _rand_idx(N, K, E, seed=11, p_mask=0.1)
+    x = ei.make_x(N, H, seed=12)
+    w = ei.uniform01(ei.stream_key(13, 0), N * K).reshape(N, K).astype(np.float32)
+    st = _status()
+    lay = ep.get_dispatch_layout(to_dev(idx), E, R, status=st)
+    _layout_equal(lay, oracle.layout(idx, E, R))
+    res = ep.dispatch(to_dev_bf16(x), lay, to_dev(w), use_fp8=use_fp8, status=st)
+    ref = oracle.dispatch(x, idx, w, E, R, use_fp8)
+    _check_dispatch(res, ref, use_fp8, K)
+    y = ep.dispatch(to_dev_bf16(x), lay, to_dev(w), with_rank=False).expert_x
+    out = ep.combine(y, lay, to_dev(w), status=st)
+    ref_out, _ = oracle.combine(u16(y), ref["layout"]["expert_slot"], w)
+    assert np.array_equal(u16(out), ref_out)
+    assert status_value(st) == 0
+
+
 def test_dispatch_expert_only_and_rank_only():
     cfg = ei.CONFIGS[4].scaled(N=500, H=1024)
     d = ei.make_inputs(cfg, seed=9)
