@@ -20,8 +20,8 @@
 // scheduler hands out blocks as earlier ones retire, which balances tokens
 // with many copies against tokens with few.
 // FP8: bulk TMA in, quantised in place in shared memory, bulk TMA out (see
-// dispatch_fp8_kernel below), again one token per warp and one bulk store
-// per destination row.
+// dispatch_fp8_kernel below): one token per block of four warps, one bulk
+// store per destination row.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -127,20 +127,22 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
 }
 
 // ---- FP8 dispatch ---------------------------------------------------------------
-// A warp per token, one warp per block. Lane 0 brings the token's BF16 row
-// into shared memory with one bulk TMA load (so the whole row is in flight
-// at once); the warp then quantises it in place, 512 channels per step:
-// lanes own 16 consecutive channels (8 lanes = one 128-channel block), take
-// the block's max by shuffles, divide by the scale (IEEE) and convert to
-// E4M3, writing the codes over the front of the staged row (step c0 writes
-// bytes [c0, c0 + 512), which no later step reads). Each destination row then
-// leaves by one bulk store (cp.async.bulk shared->global) issued by the lane
-// that owns it, and the scales follow with plain stores (a UE8M0 scale row is
-// not a multiple of 16 bytes). At 14.7 KB of shared memory per warp about 14
-// tokens are in flight per SM. Measured on GB300 against loading the row
-// through registers one step ahead (each token then waits out ~14 load
-// latencies behind the write traffic), against a separate E4M3 row (fewer
-// tokens in flight) and against four warps per block.
+// A block of four warps per token. Thread 0 brings the token's BF16 row into
+// shared memory with one bulk TMA load (the whole row in flight at once); the
+// warps then quantise it in place, 512 channels per warp per step: lanes own
+// 16 consecutive channels (8 lanes = one 128-channel block), take the block's
+// max by shuffles, divide by the scale (IEEE) and convert to E4M3, writing the
+// codes over the front of the staged row. Each destination row then leaves by
+// one bulk store (cp.async.bulk shared->global), and the scales follow with
+// plain stores (a UE8M0 scale row is not a multiple of 16 bytes). At 14.9 KB
+// of shared memory per token about 14 tokens are in flight per SM.
+// Measured on GB300 (all bit-identical): the row loaded through registers one
+// step ahead (each token then waits out ~14 load latencies behind the write
+// traffic); a separate E4M3 row (fewer tokens in flight); one warp per token
+// (each token's chain of load, quantisation and stores is longer, so the
+// kernel's ramp and tail are too: four warps took the 4096-token FP8
+// dispatches from 90.1 to 86.0 us and 79.9 to 74.2 us).
+constexpr int kF8Warps = 4;                  // warps per token (one token per block)
 constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank copies
 
 // Smallest power of two >= s for s >= 0 (exact on the bit pattern; a
@@ -261,9 +263,10 @@ __device__ __forceinline__ int f8_destinations(const DispatchParams& p, int64_t 
 // programmatic dependent pair), so the row's load and quantisation overlap
 // the layout. Otherwise the lookups go first, while the row is in flight.
 template <bool kLateDest>
-__global__ void __launch_bounds__(32) dispatch_fp8_kernel(const DispatchParams p) {
+__global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const DispatchParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31;
+  __shared__ int s_n, s_ne, s_ok;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int H = p.H, K = p.K;
   const int nsc = H / 128;
   const int64_t t = blockIdx.x;  // one token per block
@@ -273,38 +276,49 @@ __global__ void __launch_bounds__(32) dispatch_fp8_kernel(const DispatchParams p
   float* scales = reinterpret_cast<float*>(row + f8_row_bytes(H));
   int32_t* drow = reinterpret_cast<int32_t*>(scales + nsc);
   const unsigned xbytes = static_cast<unsigned>(H) * 2u;
-  if (lane == 0) {
+  if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(bar, xbytes);
     bulk_g2s(row, p.x + t * H, xbytes, bar);
   }
-  __syncwarp();
+  // Warp 0 looks up the destinations (all 32 lanes take part).
   int e_k = -1;
   float w_k = 0.0f;
-  if (lane < K) {
+  if (w == 0 && lane < K) {
     e_k = __ldg(p.idx + t * K + lane);
     if (p.w) w_k = __ldg(p.w + t * K + lane);
   }
-  int ne = 0, n = 0;
-  if (!kLateDest) {
+  if (!kLateDest && w == 0) {
     grid_dependency_wait();
-    n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
+    int ne = 0;
+    const int n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
+    if (lane == 0) {
+      s_n = n;
+      s_ne = ne;
+    }
   }
-  if (!mbar_wait(bar, 0, p.status)) {
+  // Thread 0 alone waits for the row; the block learns the outcome together.
+  if (tid == 0) {
+    const bool ok = mbar_wait(bar, 0, p.status);
     // Timed out: give the load a bounded chance to land before the block's
     // shared memory is released (no store has been issued yet).
-    mbar_wait(bar, 0, p.status);
-    return;
+    if (!ok) mbar_wait(bar, 0, p.status);
+    s_ok = ok ? 1 : 0;
   }
-  for (int c0 = 0; c0 < H; c0 += 512) {
-    const int c = c0 + lane * 16;
+  __syncthreads();
+  if (!s_ok) return;
+  // Step c0 covers channels [c0, c0 + 512 * kF8Warps), 512 per warp. Its codes
+  // go to bytes [c0, c0 + 512 * kF8Warps) of the row, which later steps never
+  // read; the barrier keeps them from overwriting this step's own inputs.
+  for (int c0 = 0; c0 < H; c0 += 512 * kF8Warps) {
+    const int c = c0 + w * 512 + lane * 16;
     uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
     if (c < H) {
       v0 = *reinterpret_cast<const uint4*>(row + 2 * c);
       v1 = *reinterpret_cast<const uint4*>(row + 2 * c + 16);
     }
-    __syncwarp();  // every lane has read this step's channels before any code overwrites them
+    __syncthreads();
     float sc;
     const uint4 q = quantize16(v0, v1, sc, p.fp8_flags);
     if (c < H) {
@@ -312,14 +326,20 @@ __global__ void __launch_bounds__(32) dispatch_fp8_kernel(const DispatchParams p
       if ((lane & 7) == 0) scales[c >> 7] = sc;
     }
   }
-  if (kLateDest) {
+  if (kLateDest && w == 0) {
     grid_dependency_wait();
-    n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
+    int ne = 0;
+    const int n = f8_destinations(p, t, lane, e_k, w_k, drow, ne);
+    if (lane == 0) {
+      s_n = n;
+      s_ne = ne;
+    }
   }
   fence_proxy_async_smem();
-  __syncwarp();
-  // One bulk store per destination row; lane d issues row d.
-  for (int d = lane; d < n; d += 32) {
+  __syncthreads();
+  const int n = s_n, ne = s_ne;
+  // One bulk store per destination row, spread over the block's threads.
+  for (int d = tid; d < n; d += kF8Warps * 32) {
     uint8_t* base = d < ne ? p.exp_x : p.rank_x;
     bulk_s2g(base + static_cast<int64_t>(drow[d]) * H, row, static_cast<unsigned>(H));
   }
@@ -330,11 +350,12 @@ __global__ void __launch_bounds__(32) dispatch_fp8_kernel(const DispatchParams p
     if (!sbase) continue;
     const int64_t r0 = static_cast<int64_t>(drow[d]) * nsc;
     if (ue8m0)
-      for (int b = lane; b < nsc; b += 32) static_cast<uint8_t*>(sbase)[r0 + b] = ue8m0_byte(scales[b]);
+      for (int b = tid; b < nsc; b += kF8Warps * 32) static_cast<uint8_t*>(sbase)[r0 + b] = ue8m0_byte(scales[b]);
     else
-      for (int b = lane; b < nsc; b += 32) static_cast<float*>(sbase)[r0 + b] = scales[b];
+      for (int b = tid; b < nsc; b += kF8Warps * 32) static_cast<float*>(sbase)[r0 + b] = scales[b];
   }
-  // The shared row must outlive the stores' reads of it.
+  // The shared row must outlive the stores' reads of it (each thread waits
+  // for the stores it issued).
   bulk_wait_read<0>();
 }
 
@@ -365,7 +386,7 @@ cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s, bool pdl) {
   void (*fn)(DispatchParams) = pdl ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
   if (err != cudaSuccess) return err;
-  return launch_ex(fn, static_cast<unsigned>(p.N), 32, smem, s, pdl, p);
+  return launch_ex(fn, static_cast<unsigned>(p.N), kF8Warps * 32, smem, s, pdl, p);
 }
 
 cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s, bool pdl) {
