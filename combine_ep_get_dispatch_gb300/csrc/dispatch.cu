@@ -85,10 +85,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
     }
   }
 
-  if (!mbar_wait(bar, 0, p.status)) {
+  // Every lane sees the row land itself (its stores read it); the warp
+  // leaves together if any lane's bounded wait gave up.
+  const bool ok = mbar_wait(bar, 0, p.status);
+  if (!__all_sync(0xffffffffu, ok)) {
     // Timed out: give the load a bounded chance to land before the block's
     // shared memory is released (no store has been issued yet).
-    mbar_wait(bar, 0, p.status);
+    if (!ok) mbar_wait(bar, 0, p.status);
     return;
   }
 
@@ -265,7 +268,7 @@ __device__ __forceinline__ int f8_destinations(const DispatchParams& p, int64_t 
 template <bool kLateDest>
 __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const DispatchParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_n, s_ne, s_ok;
+  __shared__ int s_n, s_ne;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int H = p.H, K = p.K;
   const int nsc = H / 128;
@@ -282,6 +285,9 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
     mbar_arrive_expect_tx(bar, xbytes);
     bulk_g2s(row, p.x + t * H, xbytes, bar);
   }
+  // Every thread waits on the mbarrier below: none may touch it before
+  // thread 0 has initialised it.
+  __syncthreads();
   // Warp 0 looks up the destinations (all 32 lanes take part).
   int e_k = -1;
   float w_k = 0.0f;
@@ -298,16 +304,15 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
       s_ne = ne;
     }
   }
-  // Thread 0 alone waits for the row; the block learns the outcome together.
-  if (tid == 0) {
-    const bool ok = mbar_wait(bar, 0, p.status);
+  // Every thread sees the row land itself (it reads the row); the block
+  // leaves together if any thread's bounded wait gave up.
+  const bool ok = mbar_wait(bar, 0, p.status);
+  if (!__syncthreads_and(ok)) {
     // Timed out: give the load a bounded chance to land before the block's
     // shared memory is released (no store has been issued yet).
     if (!ok) mbar_wait(bar, 0, p.status);
-    s_ok = ok ? 1 : 0;
+    return;
   }
-  __syncthreads();
-  if (!s_ok) return;
   // Step c0 covers channels [c0, c0 + 512 * kF8Warps), 512 per warp. Its codes
   // go to bytes [c0, c0 + 512 * kF8Warps) of the row, which later steps never
   // read; the barrier keeps them from overwriting this step's own inputs.
