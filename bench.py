@@ -55,7 +55,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(ei.CONFIGS))
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(ei.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=None, help="override the token count (profiling runs)")
     ap.add_argument("--fp8-scales", default="fp32", choices=["fp32", "pow2", "ue8m0"],
                     help="FP8 workloads: fp32 scales, power-of-two fp32 scales, or UE8M0 bytes")
@@ -466,7 +466,7 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    cfg = ei.CONFIGS[args.workload]
+    cfg = ei.WORKLOADS[args.workload]
     if args.tokens:
         cfg = cfg.scaled(N=args.tokens)
     inp = ei.make_inputs(cfg, seed=0)
@@ -591,7 +591,7 @@ def run_ours(args):
     if dom == "dispatch" and not cfg.fp8 and args.workload == DEFAULT_WORKLOAD:
         traffic_full, src_hash = profile_traffic()
         if traffic_full is not None and src_hash == kernel_hash():
-            traffic = traffic_full * (N / ei.CONFIGS[DEFAULT_WORKLOAD].N)
+            traffic = traffic_full * (N / ei.WORKLOADS[DEFAULT_WORKLOAD].N)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -672,7 +672,7 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    cfg = ei.CONFIGS[args.workload]
+    cfg = ei.WORKLOADS[args.workload]
     sub = _sample(cfg, 256)
     n_tok = sub["n_tok"]
     for _ in range(args.warmup):

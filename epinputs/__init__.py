@@ -30,7 +30,7 @@ from typing import Dict, Optional
 import numpy as np
 
 __all__ = [
-    "Config", "CONFIGS", "splitmix64", "uniform01", "normal", "bf16_bits_from_f32",
+    "Config", "WORKLOADS", "splitmix64", "uniform01", "normal", "bf16_bits_from_f32",
     "make_x", "make_routing", "make_inputs", "stream_key",
 ]
 
@@ -139,7 +139,7 @@ class Config:
         return dataclasses.replace(self, **kw)
 
 
-CONFIGS: Dict[int, Config] = {
+WORKLOADS: Dict[int, Config] = {
     # Low-latency decode, tiny: 8 ranks x 16 tokens, BF16.
     1: Config("ll_decode_tiny_n128_h7168_e256_k8_r8", N=128, H=7168, E=256, K=8, R=8,
               fp8=False, mode="ll", routing="softmax", T=128),

@@ -32,7 +32,7 @@ def _expert_outputs(shape, seed):
 def test_two_phase_ll_combine(c, n_s, H):
     # T = 32 only sizes the fixed regions (rows are packed from 0), and keeps
     # the host copy of the [E, R*T, H] expert outputs small.
-    cfg = ei.CONFIGS[c].scaled(N=ei.CONFIGS[c].R * n_s, H=H, T=32)
+    cfg = ei.WORKLOADS[c].scaled(N=ei.WORKLOADS[c].R * n_s, H=H, T=32)
     d = ei.make_inputs(cfg, seed=c + 20)
     st = _status()
     recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), cfg.T, cfg.E,
@@ -53,7 +53,7 @@ def test_two_phase_ll_combine(c, n_s, H):
 
 def test_ll_path_in_a_cuda_graph():
     """send + receive + combine captured once, replayed on two batches."""
-    cfg = ei.CONFIGS[1].scaled(H=2048)
+    cfg = ei.WORKLOADS[1].scaled(H=2048)
     N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
     x = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
@@ -96,7 +96,7 @@ def test_ll_path_in_a_cuda_graph():
 
 def test_normal_path_in_a_cuda_graph():
     """layout + dispatch (worst-case capacities) + combine captured once, replayed on two batches."""
-    cfg = ei.CONFIGS[3].scaled(N=512, H=1024)
+    cfg = ei.WORKLOADS[3].scaled(N=512, H=1024)
     N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
     x = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
@@ -144,7 +144,7 @@ def test_normal_path_in_a_cuda_graph():
 def test_layout_dispatch_pair_in_a_cuda_graph():
     """ep_layout_dispatch (a programmatic-dependent pair of launches) + combine
     captured once, replayed on two batches."""
-    cfg = ei.CONFIGS[5].scaled(N=700, H=1024)
+    cfg = ei.WORKLOADS[5].scaled(N=700, H=1024)
     N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
     x = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((N, K), dtype=torch.int32, device="cuda")
@@ -202,7 +202,7 @@ def test_overlapped_launches_back_to_back():
     steps = 10
     st = _status()
     # low latency
-    cfg = ei.CONFIGS[1].scaled(H=1024)
+    cfg = ei.WORKLOADS[1].scaled(H=1024)
     N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
     ins = [ei.make_inputs(cfg, seed=70 + i) for i in range(steps)]
     xs = [to_dev_bf16(d["x"]) for d in ins]
@@ -228,7 +228,7 @@ def test_overlapped_launches_back_to_back():
         ref_out, _ = oracle.ll_combine(ref["recv_x"], ref["slot_map"], d["topk_weights"])
         assert np.array_equal(u16(outs[i]), ref_out)
     # normal mode, layout + FP8 dispatch in one call, then combine of the BF16 rows
-    cfg = ei.CONFIGS[3].scaled(N=300, H=512)
+    cfg = ei.WORKLOADS[3].scaled(N=300, H=512)
     N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
     ins = [ei.make_inputs(cfg, seed=80 + i) for i in range(steps)]
     ws = torch.zeros(ep.ep_layout_workspace_bytes(N, K, E, R), dtype=torch.uint8, device="cuda")
@@ -258,7 +258,7 @@ def test_overlapped_launches_back_to_back():
 
 @pytest.mark.parametrize("round_scale,ue8m0", [(True, False), (False, True)])
 def test_dispatch_power_of_two_and_ue8m0_scales(round_scale, ue8m0):
-    cfg = ei.CONFIGS[5].scaled(N=700, H=4096)
+    cfg = ei.WORKLOADS[5].scaled(N=700, H=4096)
     d = ei.make_inputs(cfg, seed=50)
     # a few tokens with tiny magnitudes exercise the UE8M0 floor of 2^-127
     x = d["x"].copy()
@@ -279,7 +279,7 @@ def test_dispatch_power_of_two_and_ue8m0_scales(round_scale, ue8m0):
 
 
 def test_ll_ue8m0_and_cumulative_receive_stats():
-    cfg = ei.CONFIGS[2].scaled(N=32 * 16, H=1024)
+    cfg = ei.WORKLOADS[2].scaled(N=32 * 16, H=1024)
     stats = torch.zeros(cfg.E, dtype=torch.int32, device="cuda")
     total = np.zeros(cfg.E, np.int64)
     for seed in (60, 61):
@@ -302,7 +302,7 @@ def test_ll_ue8m0_and_cumulative_receive_stats():
 
 
 def test_combine_with_shared_expert_bias():
-    cfg = ei.CONFIGS[3].scaled(N=600, H=2048)
+    cfg = ei.WORKLOADS[3].scaled(N=600, H=2048)
     idx, w = ei.make_routing(cfg, seed=70)
     lay_ref = oracle.layout(idx, cfg.E, cfg.R)
     D_e = int(lay_ref["expert_offset"][-1])
@@ -314,7 +314,7 @@ def test_combine_with_shared_expert_bias():
     ref, _ = oracle.combine(y, lay_ref["expert_slot"], w, bias)
     assert np.array_equal(u16(out), ref)
     # low latency, one launch and two phases
-    lcfg = ei.CONFIGS[1].scaled(H=1024)
+    lcfg = ei.WORKLOADS[1].scaled(H=1024)
     d = ei.make_inputs(lcfg, seed=72)
     recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), lcfg.T, lcfg.E,
                                                       lcfg.R, use_fp8=False, status=st)
@@ -332,7 +332,7 @@ def test_combine_with_shared_expert_bias():
 
 @pytest.mark.parametrize("A,fp8,ue8m0", [(128, False, False), (128, True, False), (2, True, True)])
 def test_aligned_expert_layout_and_zero_padding(A, fp8, ue8m0):
-    cfg = ei.CONFIGS[5].scaled(N=900, H=1024)
+    cfg = ei.WORKLOADS[5].scaled(N=900, H=1024)
     d = ei.make_inputs(cfg, seed=80)
     st = _status()
     lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R, status=st, expert_alignment=A)
@@ -359,7 +359,7 @@ def test_aligned_expert_layout_and_zero_padding(A, fp8, ue8m0):
 
 
 def test_two_level_combine_matches_oracle():
-    cfg = ei.CONFIGS[3].scaled(N=800, H=1024)
+    cfg = ei.WORKLOADS[3].scaled(N=800, H=1024)
     idx, w = ei.make_routing(cfg, seed=90)
     lay_ref = oracle.layout(idx, cfg.E, cfg.R)
     D_e = int(lay_ref["expert_offset"][-1])
@@ -376,7 +376,7 @@ def test_two_level_combine_matches_oracle():
 
 
 def test_dispatch_and_combine_backward():
-    cfg = ei.CONFIGS[4].scaled(N=700, H=2048)
+    cfg = ei.WORKLOADS[4].scaled(N=700, H=2048)
     d = ei.make_inputs(cfg, seed=100)
     idx, w = d["topk_idx"], d["topk_weights"]
     lay_ref = oracle.layout(idx, cfg.E, cfg.R)
@@ -430,7 +430,7 @@ def test_shrink_mask_buffer_update_query_clean():
 def test_shrink_send_and_combine(c, n_s, H, T):
     """Ranks masked before the send drop out of the receive buffers; a rank lost
     between send and combine is skipped by the one- and the two-phase combine."""
-    cfg = ei.CONFIGS[c].scaled(N=ei.CONFIGS[c].R * n_s, H=H, T=T)
+    cfg = ei.WORKLOADS[c].scaled(N=ei.WORKLOADS[c].R * n_s, H=H, T=T)
     N, K, E, R, T = cfg.N, cfg.K, cfg.E, cfg.R, cfg.T
     d = ei.make_inputs(cfg, seed=c + 70)
     st = _status()

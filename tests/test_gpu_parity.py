@@ -44,7 +44,7 @@ def _layout_equal(lay, ref):
 # ------------------------------------------------------------------ layout ----
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
 def test_layout_full_configs(c):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     idx, _ = ei.make_routing(cfg, 0)
     st = _status()
     lay = ep.get_dispatch_layout(to_dev(idx), cfg.E, cfg.R, status=st)
@@ -102,7 +102,7 @@ def test_layout_all_masked_and_bad_indices():
 
 
 def test_layout_deterministic_repeat():
-    cfg = ei.CONFIGS[4]
+    cfg = ei.WORKLOADS[4]
     idx, _ = ei.make_routing(cfg, 0)
     a = ep.get_dispatch_layout(to_dev(idx), cfg.E, cfg.R)
     b = ep.get_dispatch_layout(to_dev(idx), cfg.E, cfg.R)
@@ -114,7 +114,7 @@ def test_layout_workspace_left_clean_and_dirty_one_flagged():
     """The grid barrier clears its own arrival count: calls on one zero-filled
     workspace stay exact with no reset in between; a leftover count (a
     workspace never zero-filled) is reported with EP_ST_WORKSPACE."""
-    cfg = ei.CONFIGS[4].scaled(N=2048)          # 12288 entries: a dozen CTAs, so a real grid barrier
+    cfg = ei.WORKLOADS[4].scaled(N=2048)          # 12288 entries: a dozen CTAs, so a real grid barrier
     idx, _ = ei.make_routing(cfg, 50)
     ref = oracle.layout(idx, cfg.E, cfg.R)
     ws = torch.zeros(ep.ep_layout_workspace_bytes(cfg.N, cfg.K, cfg.E, cfg.R), dtype=torch.uint8, device="cuda")
@@ -162,7 +162,7 @@ def _check_dispatch(res, ref, use_fp8, K, with_rank=True):
 def test_dispatch_parity(c, N, H, use_fp8):
     if use_fp8 and H % 128:
         pytest.skip("FP8 needs hidden % 128 == 0")
-    cfg = ei.CONFIGS[c].scaled(N=N, H=H)
+    cfg = ei.WORKLOADS[c].scaled(N=N, H=H)
     d = ei.make_inputs(cfg, seed=c)
     st = _status()
     lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R, status=st)
@@ -196,7 +196,7 @@ def test_maximum_sizes(use_fp8):
 
 
 def test_dispatch_expert_only_and_rank_only():
-    cfg = ei.CONFIGS[4].scaled(N=500, H=1024)
+    cfg = ei.WORKLOADS[4].scaled(N=500, H=1024)
     d = ei.make_inputs(cfg, seed=9)
     lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R)
     ref = oracle.dispatch(d["x"], d["topk_idx"], d["topk_weights"], cfg.E, cfg.R, False)
@@ -213,7 +213,7 @@ def test_dispatch_expert_only_and_rank_only():
 def test_layout_and_dispatch_in_one_call(c, N, H, use_fp8):
     """ep_layout_dispatch (the dispatch launched as the layout's programmatic
     dependent) gives the oracle's layout and receive rows."""
-    cfg = ei.CONFIGS[c].scaled(N=N, H=H)
+    cfg = ei.WORKLOADS[c].scaled(N=N, H=H)
     d = ei.make_inputs(cfg, seed=c + 20)
     st = _status()
     lay, res = ep.get_layout_and_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), cfg.E, cfg.R,
@@ -240,7 +240,7 @@ def _same_dispatch(lay1, r1, lay2, r2):
 def test_layout_and_dispatch_full_size_matches_two_calls(c):
     """On the full workloads the one-call path writes exactly what
     ep_get_dispatch_layout + ep_dispatch write (checked against the oracle above)."""
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     d = ei.make_inputs(cfg, seed=0)
     x, idx, w = to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
     st = _status()
@@ -267,7 +267,7 @@ def test_layout_and_dispatch_empty_masked_and_bad_indices():
     idx[::7, 1] = 32
     idx[::11, 2] = -5
     idx[::13, 3] = -1
-    d = ei.make_inputs(ei.CONFIGS[4].scaled(N=500, H=H, K=4, E=32, R=4), seed=6)
+    d = ei.make_inputs(ei.WORKLOADS[4].scaled(N=500, H=H, K=4, E=32, R=4), seed=6)
     x, w = to_dev_bf16(d["x"]), to_dev(d["topk_weights"])
     for fp8 in (False, True):
         st1, st2 = _status(), _status()
@@ -281,7 +281,7 @@ def test_layout_and_dispatch_empty_masked_and_bad_indices():
 
 def test_layout_and_dispatch_aligned_with_padding():
     """Expert segments padded to 128 rows: padding rows are zero-filled by the one-call path too."""
-    cfg = ei.CONFIGS[3].scaled(N=600, H=1024)
+    cfg = ei.WORKLOADS[3].scaled(N=600, H=1024)
     d = ei.make_inputs(cfg, seed=31)
     x, idx, w = to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
     st = _status()
@@ -293,7 +293,7 @@ def test_layout_and_dispatch_aligned_with_padding():
 
 
 def test_dispatch_capacity_overflow_flagged():
-    cfg = ei.CONFIGS[4].scaled(N=400, H=256)
+    cfg = ei.WORKLOADS[4].scaled(N=400, H=256)
     d = ei.make_inputs(cfg, seed=4)
     lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R)
     D_e = int(lay.expert_offset[-1].item())
@@ -317,7 +317,7 @@ def _expert_outputs(n_rows, H, seed):
 @pytest.mark.parametrize("c,N,H", [(3, 1000, 7168), (4, 777, 7168), (5, 1500, 4096), (4, 129, 8),
                                    (5, 100, 1032)])
 def test_combine_parity(c, N, H):
-    cfg = ei.CONFIGS[c].scaled(N=N, H=H)
+    cfg = ei.WORKLOADS[c].scaled(N=N, H=H)
     idx, w = ei.make_routing(cfg, seed=c + 10)
     lay_ref = oracle.layout(idx, cfg.E, cfg.R)
     D_e = int(lay_ref["expert_offset"][-1])
@@ -333,7 +333,7 @@ def test_combine_parity(c, N, H):
 
 
 def test_combine_identity_round_trip():
-    cfg = ei.CONFIGS[4].scaled(N=600, H=2048)
+    cfg = ei.WORKLOADS[4].scaled(N=600, H=2048)
     d = ei.make_inputs(cfg, seed=5)
     lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R)
     x = to_dev_bf16(d["x"])
@@ -363,7 +363,7 @@ def test_combine_masked_and_capacity():
 # ------------------------------------------------------- full-size samples ----
 @pytest.mark.parametrize("c", [3, 4, 5])
 def test_full_size_sampled(c):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     d = ei.make_inputs(cfg, seed=0)
     st = _status()
     x = to_dev_bf16(d["x"])
@@ -414,7 +414,7 @@ def test_full_size_sampled(c):
 def test_ll_dispatch_parity(c, n_s, H, T):
     # T only sizes the fixed regions (packed rows do not depend on it); the
     # full-width case uses a small T so the oracle's host buffers stay small.
-    base = ei.CONFIGS[c]
+    base = ei.WORKLOADS[c]
     cfg = base.scaled(N=base.R * n_s, H=H, T=T)
     use_fp8 = cfg.fp8
     d = ei.make_inputs(cfg, seed=c + n_s)
@@ -454,7 +454,7 @@ def test_ll_dispatch_parity(c, n_s, H, T):
 
 @pytest.mark.parametrize("c", [1, 2])
 def test_ll_full_size(c):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     d = ei.make_inputs(cfg, seed=0)
     st = _status()
     x = to_dev_bf16(d["x"])
@@ -498,7 +498,7 @@ def test_ll_full_size(c):
 
 
 def test_ll_receive_without_send_and_mismatch():
-    cfg = ei.CONFIGS[1].scaled(H=256)
+    cfg = ei.WORKLOADS[1].scaled(H=256)
     N, K, E, R, T = cfg.N, cfg.K, cfg.E, cfg.R, cfg.T
     ws = torch.zeros(ep.ep_ll_workspace_bytes(N, K, E, R, T), dtype=torch.uint8, device="cuda")
     cnt = torch.full((E,), -7, dtype=torch.int32, device="cuda")
@@ -524,7 +524,7 @@ def test_ll_receive_without_send_and_mismatch():
 
 
 def test_ll_capacity_is_a_host_error():
-    cfg = ei.CONFIGS[1].scaled(H=256, N=8 * 20)
+    cfg = ei.WORKLOADS[1].scaled(H=256, N=8 * 20)
     d = ei.make_inputs(cfg, seed=1)
     with pytest.raises(ep.EPError) as ei_:
         ep.low_latency_dispatch(to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), 16, cfg.E, cfg.R, use_fp8=False)
@@ -532,7 +532,7 @@ def test_ll_capacity_is_a_host_error():
 
 
 def test_ll_hook_on_another_stream_ordered_by_event():
-    cfg = ei.CONFIGS[1].scaled(H=512)
+    cfg = ei.WORKLOADS[1].scaled(H=512)
     d = ei.make_inputs(cfg, seed=6)
     x = to_dev_bf16(d["x"])
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()

@@ -35,7 +35,7 @@ def test_bf16_bits_roundtrip_nearest():
 
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
 def test_routing_shapes_and_determinism(c):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     i1, w1 = ei.make_routing(cfg, 0)
     i2, w2 = ei.make_routing(cfg, 0)
     assert i1.shape == (cfg.N, cfg.K) and i1.dtype == np.int32
@@ -56,14 +56,14 @@ def test_routing_shapes_and_determinism(c):
 
 
 def test_grouped_gating_limits_groups():
-    cfg = ei.CONFIGS[3]
+    cfg = ei.WORKLOADS[3]
     idx, _ = ei.make_routing(cfg, 0)
     groups = idx // (cfg.E // cfg.n_groups)
     assert max(len(set(r)) for r in groups.tolist()) <= cfg.topk_groups
 
 
 def test_zipf_mask_and_skew():
-    cfg = ei.CONFIGS[5]
+    cfg = ei.WORKLOADS[5]
     idx, w = ei.make_routing(cfg, 0)
     n_mask = int(round(cfg.mask_frac * cfg.N * cfg.K))
     assert (idx == -1).sum() == n_mask == 6554

@@ -25,7 +25,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _small(c, N=None, H=None, **kw):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     return cfg.scaled(N=N or cfg.N, H=H or cfg.H, **kw)
 
 
@@ -83,7 +83,7 @@ def test_dispatch_fp8_rows_are_quantised_source_rows():
 
 def test_volume_example():
     g = json.load(open(os.path.join(GOLDEN, "volume_example.json")))
-    cfg = ei.CONFIGS[4]
+    cfg = ei.WORKLOADS[4]
     assert (cfg.N, cfg.H, cfg.K) == (g["num_tokens"], g["hidden"], g["copies"])
     idx, w = ei.make_routing(cfg, 0)
     lay = oracle.layout(idx, cfg.E, cfg.R)
@@ -188,7 +188,7 @@ def test_masked_slots_skipped_and_all_masked_is_positive_zero():
 
 @pytest.mark.parametrize("c,use_fp8", [(1, False), (2, True)])
 def test_ll_matches_layout_and_expert_major(c, use_fp8):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     n_s = 16 if c == 1 else 8
     cfg = cfg.scaled(N=cfg.R * n_s, H=256)
     x, idx, w = _inputs(cfg)
@@ -223,7 +223,7 @@ def test_ll_matches_layout_and_expert_major(c, use_fp8):
 
 
 def test_ll_combine_identity():
-    cfg = ei.CONFIGS[1].scaled(H=512)
+    cfg = ei.WORKLOADS[1].scaled(H=512)
     x, idx, w = _inputs(cfg)
     ll = oracle.ll_dispatch(x, idx, cfg.E, cfg.R, cfg.T, False)
     out, st = oracle.ll_combine(ll["recv_x"], ll["slot_map"], w)
@@ -234,7 +234,7 @@ def test_ll_combine_identity():
 
 
 def test_ll_overflow_flagged():
-    cfg = ei.CONFIGS[1].scaled(H=128, N=8 * 20)
+    cfg = ei.WORKLOADS[1].scaled(H=128, N=8 * 20)
     x, idx, w = _inputs(cfg)
     ll = oracle.ll_dispatch(x, idx, cfg.E, cfg.R, 16, False)
     assert ll["status"] & oracle.LL_OVERFLOW
@@ -244,7 +244,7 @@ def test_two_phase_ll_combine_equals_single_phase():
     # Send half: every routed (t, k) row lands at staging row t*K + k, a copy
     # of y's row; receive half: the same weighted sum as the one-launch combine
     # ("DeepEP V1 guide" 6.1: low_latency_combine with a receive hook).
-    cfg = ei.CONFIGS[2].scaled(N=32 * 8, H=256)
+    cfg = ei.WORKLOADS[2].scaled(N=32 * 8, H=256)
     x, idx, w = _inputs(cfg, seed=4)
     ll = oracle.ll_dispatch(x, idx, cfg.E, cfg.R, cfg.T, False)
     y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(9, 3), ll["recv_x"].size).astype(np.float32))
@@ -289,7 +289,7 @@ def test_shrink_mask_hand_example():
 
 
 def test_shrink_mask_degenerate_cases():
-    cfg = ei.CONFIGS[2].scaled(N=32 * 8, H=256)
+    cfg = ei.WORKLOADS[2].scaled(N=32 * 8, H=256)
     x, idx, w = _inputs(cfg, seed=6)
     R, E, T = cfg.R, cfg.E, cfg.T
     plain = oracle.ll_dispatch(x, idx, E, R, T, True)

@@ -53,7 +53,7 @@ def test_lesson14_table():
 
 @pytest.mark.parametrize("c", [1, 2, 3, 4, 5])
 def test_invariants_on_configs(c):
-    cfg = ei.CONFIGS[c]
+    cfg = ei.WORKLOADS[c]
     idx, _ = ei.make_routing(cfg, 0)
     E, R, N, K = cfg.E, cfg.R, cfg.N, cfg.K
     L = E // R

@@ -48,7 +48,7 @@ def _call(f, lay, status):
 @pytest.mark.parametrize("cfgs", [(4, 5), (3, 2)])
 def test_noalloc_matches_workspace_entry_point_twice(noalloc, cfgs):
     for c in cfgs:  # two calls in a row on different routings
-        cfg = ei.CONFIGS[c]
+        cfg = ei.WORKLOADS[c]
         idx, _ = ei.make_routing(cfg, seed=11 + c)
         idx_d = torch.from_numpy(idx).cuda()
         st_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
