@@ -244,7 +244,8 @@ def test_two_phase_ll_combine_equals_single_phase():
     # Send half: every routed (t, k) row lands at staging row t*K + k, a copy
     # of y's row; receive half: the same weighted sum as the one-launch combine
     # ("DeepEP V1 guide" 6.1: low_latency_combine with a receive hook).
-    cfg = ei.WORKLOADS[2].scaled(N=32 * 8, H=256)
+    # T = 8 fits the 8 tokens per rank; the packed rows do not depend on T.
+    cfg = ei.WORKLOADS[2].scaled(N=32 * 8, H=256, T=8)
     x, idx, w = _inputs(cfg, seed=4)
     ll = oracle.ll_dispatch(x, idx, cfg.E, cfg.R, cfg.T, False)
     y = ei.bf16_bits_from_f32(ei.normal(ei.stream_key(9, 3), ll["recv_x"].size).astype(np.float32))
@@ -289,7 +290,7 @@ def test_shrink_mask_hand_example():
 
 
 def test_shrink_mask_degenerate_cases():
-    cfg = ei.WORKLOADS[2].scaled(N=32 * 8, H=256)
+    cfg = ei.WORKLOADS[2].scaled(N=32 * 8, H=256, T=8)
     x, idx, w = _inputs(cfg, seed=6)
     R, E, T = cfg.R, cfg.E, cfg.T
     plain = oracle.ll_dispatch(x, idx, E, R, T, True)
