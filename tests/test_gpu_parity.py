@@ -279,15 +279,18 @@ def test_layout_and_dispatch_empty_masked_and_bad_indices():
         _layout_equal(lay2, oracle.layout(idx, 32, 4))
 
 
-def test_layout_and_dispatch_aligned_with_padding():
-    """Expert segments padded to 128 rows: padding rows are zero-filled by the one-call path too."""
+@pytest.mark.parametrize("round_scale,ue8m0", [(False, False), (True, False), (False, True)])
+def test_layout_and_dispatch_aligned_with_padding(round_scale, ue8m0):
+    """Expert segments padded to 128 rows, with each FP8 scale format: the
+    one-call path writes the same rows, scales and zero-filled padding rows."""
     cfg = ei.WORKLOADS[3].scaled(N=600, H=1024)
     d = ei.make_inputs(cfg, seed=31)
     x, idx, w = to_dev_bf16(d["x"]), to_dev(d["topk_idx"]), to_dev(d["topk_weights"])
     st = _status()
+    opts = dict(use_fp8=True, round_scale=round_scale, use_ue8m0=ue8m0)
     lay1 = ep.get_dispatch_layout(idx, cfg.E, cfg.R, status=st, expert_alignment=128)
-    r1 = ep.dispatch(x, lay1, w, use_fp8=True, status=st)
-    lay2, r2 = ep.get_layout_and_dispatch(x, idx, cfg.E, cfg.R, w, use_fp8=True, status=st, expert_alignment=128)
+    r1 = ep.dispatch(x, lay1, w, status=st, **opts)
+    lay2, r2 = ep.get_layout_and_dispatch(x, idx, cfg.E, cfg.R, w, status=st, expert_alignment=128, **opts)
     _same_dispatch(lay1, r1, lay2, r2)
     assert status_value(st) == 0
 
