@@ -26,7 +26,10 @@
  *     the host. Outputs are ready when the stream reaches that point.
  *   - Return value: EP_OK, or a negative EP_ERR_* code for an error the host
  *     can see (bad argument, bad alignment, too-small workspace, a CUDA
- *     launch error). Nothing is enqueued when an error is returned.
+ *     launch error). Nothing is enqueued when an argument error is returned.
+ *     A call that makes two launches (the low-latency send, layout +
+ *     dispatch in one call, an aligned dispatch with its padding fill) may
+ *     have enqueued the first when the second fails with EP_ERR_CUDA.
  *   - `status` (may be NULL) points to one device int32. Kernels OR EP_ST_*
  *     bits into it for data-dependent conditions (an expert index out of
  *     range, a destination row beyond a buffer's capacity, ...). The
