@@ -70,6 +70,8 @@ def parse():
                     help="low-latency workloads: combine in one launch, or send + receive hook")
     ap.add_argument("--mask-ranks", default="",
                     help="low-latency workloads: comma-separated ranks masked in the workspace (shrink mode)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured once in a CUDA graph and replayed (reported as `graph`)")
     ap.add_argument("--fused-layout", action="store_true",
                     help="normal workloads: layout and dispatch through one call (ep_layout_dispatch), timed as one phase")
     ap.add_argument("--no-e2e", action="store_true")
@@ -510,6 +512,36 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {st}: {ep.ep_error_string(st)}")
 
+    # The same step captured once in a CUDA graph and replayed K times (the
+    # launches of a step then cost one graph launch); L2 flushed before each
+    # replay, CUDA events around it. Reported beside the eager numbers.
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            wl.run(side, wl.x, lay, wl.w)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            wl.run(torch.cuda.current_stream(dev), wl.x, lay, wl.w)
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            gev[i][0].record(stream)
+            g.replay()
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        g_ms = float(np.mean([a.elapsed_time(b) for a, b in gev]))
+        g_ms = max_over_ranks([g_ms], dev, world)[0]
+        graph = {"ms_per_step": round(g_ms, 4), "value": round(job_throughput(cfg.N, world, g_ms), 1),
+                 "unit": "tokens/s"}
+        st = int(wl.status.item())
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {ep.ep_error_string(st)}")
+
     # End to end through the C ABI from pinned host memory, pipelined as a
     # serving loop runs it: while step i computes, step i+1's inputs go up on
     # one stream and step i-1's output comes down on another (two sets of
@@ -608,6 +640,7 @@ def run_ours(args):
                 "see epinputs for the grouped and Zipf recipes)",
         "config": workload_config(cfg, args, world, wl.rows()),
         "phases": phases,
+        **({"graph": graph} if graph else {}),
         "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind},
