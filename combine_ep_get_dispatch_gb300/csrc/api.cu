@@ -236,15 +236,25 @@ int dispatch_launch(const ep_layout_t* L, const DispatchParams& p, int fp8_flags
 
 }  // namespace
 
-extern "C" {
+namespace ep {
 
-int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status,
-                           void* stream) {
+int layout_call(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t s,
+                bool reset_barrier) {
   LayoutParams p;
   int G = 0;
   const int rc = layout_setup(L, workspace, workspace_bytes, status, p, G);
   if (rc != EP_OK) return rc;
-  return cuda_rc(launch_layout(p, G, true, false, static_cast<cudaStream_t>(stream)));
+  if (reset_barrier && cudaMemsetAsync(p.ws_barrier, 0, 256, s) != cudaSuccess) return EP_ERR_CUDA;
+  return cuda_rc(launch_layout(p, G, true, false, s));
+}
+
+}  // namespace ep
+
+extern "C" {
+
+int ep_get_dispatch_layout(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status,
+                           void* stream) {
+  return ep::layout_call(L, workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream), false);
 }
 
 int ep_dispatch(const ep_layout_t* L, const void* x, int hidden, int fp8_flags, const float* topk_weights,

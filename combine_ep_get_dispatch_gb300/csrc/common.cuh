@@ -15,9 +15,21 @@
 
 namespace ep {
 
-// Spin limits. A wait that exceeds its limit sets EP_ST_TIMEOUT and returns;
-// no kernel of this library can wait forever.
-constexpr unsigned kSpinLimit = 1u << 24;
+// Wait limits, in nanoseconds of the GPU's global timer. A wait that exceeds
+// its limit sets EP_ST_TIMEOUT and returns; no kernel of this library can
+// wait forever. Every wait here normally ends within microseconds (a row
+// landing in shared memory, the other blocks of a cooperative grid arriving),
+// so one second means something is wrong. kDrainLimitNs bounds the second
+// wait a block makes for its own bulk copy still in flight before it leaves
+// (the copy depends on no other block and lands unless its address is bad).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
+constexpr unsigned long long kDrainLimitNs = 4000000000ull;  // 4 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
@@ -59,12 +71,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
+// Bounded wait for the phase with the given parity to complete: false (and
+// EP_ST_TIMEOUT) after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int32_t* status) {
-  for (unsigned i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  flag(status, EP_ST_TIMEOUT);
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      flag(status, EP_ST_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// After a timed-out mbar_wait, before the block gives up its shared memory:
+// wait (with backoff, up to kDrainLimitNs) for the bulk load that targets it,
+// so the copy cannot land in memory a later block owns.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, unsigned parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity) && global_ns() - t0 <= kDrainLimitNs) __nanosleep(1000);
 }
 
 // ---- bulk TMA copies -----------------------------------------------------
@@ -140,8 +166,10 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 // So a workspace that was zero-filled once needs no reset between calls. A
 // block whose arrival count comes back >= nblocks found leftover words (a
 // workspace never zero-filled, or one an aborted launch left behind): it
-// flags EP_ST_WORKSPACE and does not wait. Waits are bounded: on expiry the
-// block flags EP_ST_TIMEOUT and goes on.
+// flags EP_ST_WORKSPACE and does not wait. Waits are bounded (kWaitLimitNs):
+// on expiry the block flags EP_ST_TIMEOUT and goes on; every access after
+// the barrier stays inside the caller's arrays, so the outputs are merely
+// wrong, and the status says so.
 // A relaxed read: the generation cannot change before this block arrives, so
 // no ordering is needed, and the thread does not stall on it until the wait.
 __device__ __forceinline__ unsigned barrier_generation(const unsigned* bar) {
@@ -162,9 +190,9 @@ __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, un
       __threadfence();
       atomicAdd(&bar[1], 1u);
     } else {
-      unsigned spins = 0;
+      const unsigned long long t0 = global_ns();
       while (ld_acquire_u32(bar + 1) == gen0) {
-        if (++spins > kSpinLimit) {
+        if (global_ns() - t0 > kWaitLimitNs) {
           flag(status, EP_ST_TIMEOUT);
           break;
         }

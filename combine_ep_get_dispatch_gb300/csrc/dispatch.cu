@@ -89,9 +89,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
   // leaves together if any lane's bounded wait gave up.
   const bool ok = mbar_wait(bar, 0, p.status);
   if (!__all_sync(0xffffffffu, ok)) {
-    // Timed out: give the load a bounded chance to land before the block's
-    // shared memory is released (no store has been issued yet).
-    if (!ok) mbar_wait(bar, 0, p.status);
+    // Timed out: the row load may still be in flight into this warp's
+    // shared row. Let it land (bounded) before the block can exit and its
+    // shared memory go to another block; no store has been issued yet.
+    if (lane == 0) mbar_drain(bar, 0);
+    __syncwarp();
     return;
   }
 
@@ -308,9 +310,11 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
   // leaves together if any thread's bounded wait gave up.
   const bool ok = mbar_wait(bar, 0, p.status);
   if (!__syncthreads_and(ok)) {
-    // Timed out: give the load a bounded chance to land before the block's
-    // shared memory is released (no store has been issued yet).
-    if (!ok) mbar_wait(bar, 0, p.status);
+    // Timed out: the row load may still be in flight into this block's
+    // shared row. Let it land (bounded) before the block exits and its
+    // shared memory goes to another block; no store has been issued yet.
+    if (tid == 0) mbar_drain(bar, 0);
+    __syncthreads();
     return;
   }
   // Step c0 covers channels [c0, c0 + 512 * kF8Warps), 512 per warp. Its codes

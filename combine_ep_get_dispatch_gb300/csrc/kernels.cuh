@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ep.h"
+
 namespace ep {
 
 // Workspace header of the low-latency path: written by the send, checked by
@@ -146,6 +148,12 @@ int device_sms(int dev);
 bool device_cooperative(int dev);
 cudaError_t ensure_dynamic_smem(const void* fn, int dev, size_t smem);  // raise the kernel's limit to >= smem
 int blocks_per_sm(const void* fn, int dev, int threads, size_t smem);   // occupancy, 0 on failure
+
+// The routing layout of ep_get_dispatch_layout: every check first (an error
+// code, with nothing enqueued), then, when reset_barrier is set, a zero fill
+// of the workspace's 256-byte barrier block, then the launch.
+int layout_call(const ep_layout_t* L, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t s,
+                bool reset_barrier);
 
 // Launchers: return cudaSuccess or the launch error.
 size_t layout_smem_bytes(int E, int R, bool with_rank);

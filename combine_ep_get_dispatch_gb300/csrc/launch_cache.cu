@@ -7,7 +7,8 @@
 // of a kernel fit on one SM for a given block size and shared memory, and
 // whether a kernel's dynamic shared-memory limit has already been raised. So
 // each is asked of the runtime once and remembered. The tables are guarded by
-// one mutex; the runtime calls happen outside it.
+// one mutex; the attribute and occupancy queries run outside it, the
+// shared-memory limit call inside it (see ensure_dynamic_smem).
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -63,18 +64,18 @@ bool device_cooperative(int dev) {
   return d && d->coop != 0;
 }
 
+// The check, the runtime call and the record happen under one lock: two
+// threads raising the same kernel's limit to different values must leave the
+// runtime at the value the table records (otherwise the smaller call could
+// land last while the table kept the larger one).
 cudaError_t ensure_dynamic_smem(const void* fn, int dev, size_t smem) {
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    const auto it = g_smem_limit.find({fn, dev});
-    if (it != g_smem_limit.end() && it->second >= smem) return cudaSuccess;
-  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  size_t& v = g_smem_limit[{fn, dev}];
+  if (v >= smem) return cudaSuccess;
   const cudaError_t err =
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  size_t& v = g_smem_limit[{fn, dev}];
-  if (smem > v) v = smem;
+  v = smem;
   return cudaSuccess;
 }
 

@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "ep.h"
+#include "kernels.cuh"
 
 namespace {
 
@@ -61,7 +62,8 @@ extern "C" int ep_get_dispatch_layout_noalloc(const ep_layout_t* L, int32_t* sta
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != EP_OK) return rc;
-  // The layout workspace starts with its 256-byte barrier block.
-  if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return EP_ERR_CUDA;
-  return ep_get_dispatch_layout(L, scratch, kStaticScratchBytes, status, stream);
+  // The same checks as ep_get_dispatch_layout come first, so an argument
+  // error enqueues nothing; then the array's 256-byte barrier block is
+  // zeroed on the stream, then the layout runs.
+  return ep::layout_call(L, scratch, kStaticScratchBytes, status, static_cast<cudaStream_t>(stream), true);
 }

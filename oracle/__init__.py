@@ -24,15 +24,38 @@ import numpy as np
 
 from . import build as _build
 
-_lib = None
+_libs = {}
+_all_cores = False
+
+
+def use_all_cores(on: bool = True) -> bool:
+    """Route the oracle's calls to the all-core build (the same source
+    compiled with OpenMP; identical results) or back to the plain
+    single-threaded one. Returns False, and stays on the plain build, when no
+    all-core build is available. Only the benchmark's CPU-baseline timing
+    uses it."""
+    global _all_cores
+    if on and _build.build_omp() is None:
+        _all_cores = False
+        return False
+    _all_cores = on
+    return True
+
+
+def threads() -> int:
+    """Threads the loaded oracle's row loops use (1 for the plain build)."""
+    return int(lib().oracle_threads())
 
 
 def lib():
-    global _lib
-    if _lib is None:
-        # EP_ORACLE_LIB: a prebuilt oracle library to load instead (the
-        # mutation test points it at deliberately broken copies).
-        path = os.environ.get("EP_ORACLE_LIB") or _build.build()
+    key = "omp" if _all_cores else "plain"
+    if key not in _libs:
+        if key == "omp":
+            path = _build.build_omp()
+        else:
+            # EP_ORACLE_LIB: a prebuilt oracle library to load instead (the
+            # mutation test points it at deliberately broken copies).
+            path = os.environ.get("EP_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         P = ctypes.c_void_p
         i32, i64 = ctypes.c_int, ctypes.c_int64
@@ -72,8 +95,10 @@ def lib():
         L.oracle_ll_mask_routing.restype = i32
         L.oracle_ll_mask_slot_map.argtypes = [P, i32, i32, i32, i32, i32, P, P]
         L.oracle_ll_mask_slot_map.restype = i32
-        _lib = L
-    return _lib
+        L.oracle_threads.argtypes = []
+        L.oracle_threads.restype = i32
+        _libs[key] = L
+    return _libs[key]
 
 
 # Status bits returned by the oracle.

@@ -37,9 +37,17 @@
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -shared -fPIC.
 // The only fused multiply-add is the explicit std::fmaf of the combine.
+// A second build of this same file with -fopenmp (libep_oracle_omp.so) runs
+// the per-token row loops of dispatch and combine, and the per-expert loop of
+// the low-latency dispatch, on every host core: those iterations write
+// disjoint rows, so the results are identical; the layout stays sequential.
+// It exists only to time the oracle on all cores next to the plain build.
 
 #include <cmath>
 #include <cstdint>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <cstring>
 #include <utility>
 #include <vector>
@@ -179,6 +187,16 @@ void write_row(const uint8_t* payload, const float* scales, int H, int flags,
 
 extern "C" {
 
+// Threads the row loops use: 1 in the plain build, the OpenMP team size in
+// the all-core build (compiled from this same file with -fopenmp).
+int oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
 uint16_t oracle_bf16_from_f32(float f) { return bf16_from_f32(f); }
 uint8_t oracle_e4m3_from_f32(float f) { return e4m3_from_f32(f); }
 double oracle_e4m3_to_f64(uint8_t c) { return e4m3_to_f64(c); }
@@ -278,8 +296,14 @@ int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
   const bool use_fp8 = flags & kFp8;
   int status = 0;
   const int L = E / R;
+  // Tokens are independent (each writes only its own destination rows), so
+  // the all-core build splits this loop over threads; the plain build runs
+  // it in order. The results are the same either way.
+#pragma omp parallel reduction(| : status)
+  {
   std::vector<uint8_t> q(H);
   std::vector<float> sc(H / 128 > 0 ? H / 128 : 1);
+#pragma omp for schedule(dynamic, 16)
   for (int t = 0; t < N; ++t) {
     const uint16_t* xt = x + static_cast<int64_t>(t) * H;
     const uint8_t* payload = reinterpret_cast<const uint8_t*>(xt);
@@ -308,6 +332,7 @@ int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
       if (exp_src) exp_src[row] = t * K + k;
     }
   }
+  }
   return status;
 }
 
@@ -320,7 +345,11 @@ int oracle_dispatch(const uint16_t* x, const int32_t* idx, const float* w,
 int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const float* w,
                    const uint16_t* bias, int N, int K, int H, uint16_t* out) {
   int status = 0;
+  // Tokens are independent: split over threads in the all-core build.
+#pragma omp parallel reduction(| : status)
+  {
   std::vector<float> acc(H);
+#pragma omp for schedule(dynamic, 16)
   for (int t = 0; t < N; ++t) {
     std::fill(acc.begin(), acc.end(), 0.0f);
     for (int k = 0; k < K; ++k) {
@@ -334,6 +363,7 @@ int oracle_combine(const uint16_t* y, int64_t y_rows, const int32_t* slot, const
     if (bias)
       for (int h = 0; h < H; ++h) acc[h] = acc[h] + f32_from_bf16(bias[static_cast<int64_t>(t) * H + h]);
     for (int h = 0; h < H; ++h) out[static_cast<int64_t>(t) * H + h] = bf16_from_f32(acc[h]);
+  }
   }
   return status;
 }
@@ -461,8 +491,13 @@ int oracle_ll_dispatch(const uint16_t* x, const int32_t* idx, int N, int K, int 
       if (!valid_expert(e, E)) { status |= kBadIndex; continue; }
       expert_list[e].push_back({t, k});
     }
+  // Experts are independent (each fills only its own region): split over
+  // threads in the all-core build.
+#pragma omp parallel reduction(| : status)
+  {
   std::vector<uint8_t> q(H);
   std::vector<float> sc(H / 128 > 0 ? H / 128 : 1);
+#pragma omp for schedule(dynamic, 1)
   for (int e = 0; e < E; ++e) {
     recv_count[e] = static_cast<int32_t>(expert_list[e].size());
     std::vector<int64_t> count_from(R, 0);
@@ -484,6 +519,7 @@ int oracle_ll_dispatch(const uint16_t* x, const int32_t* idx, int N, int K, int 
       layout_range[static_cast<int64_t>(e) * R + s] = (offset << 32) | count_from[s];
       offset += count_from[s];
     }
+  }
   }
   return status;
 }

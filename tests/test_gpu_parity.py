@@ -6,8 +6,8 @@ makes it bit-exact too: the same fp32 fused multiply-add chain in slot order,
 and that is asserted as well).
 
 Sizes: ragged slices of every workload that span several CTAs and warps,
-plus the full workloads, where rows and tokens are sampled and checked one
-by one against the oracle.
+edge shapes and the maximum sizes the ABI accepts; the full workloads are
+compared array by array in test_gpu_full_size.py.
 """
 import numpy as np
 import pytest
@@ -132,6 +132,35 @@ def test_layout_workspace_left_clean_and_dirty_one_flagged():
     ep.ep_get_dispatch_layout(lay, ws, st)
     assert status_value(st) & ep.EP_ST_WORKSPACE
     ws[:8] = 0
+    st = _status()
+    ep.ep_get_dispatch_layout(lay, ws, st)
+    _layout_equal(lay, ref)
+    assert status_value(st) == 0
+
+
+def test_layout_grid_wait_runs_out_and_reports_it():
+    """A bounded in-kernel wait that runs out: the layout's arrival count is
+    seeded with 0xFFFFFFFF, so the first block to arrive sees a count above
+    the block count (EP_ST_WORKSPACE) and wraps it to zero, and no later block
+    is ever the last arrival. The others wait their one-second limit, set
+    EP_ST_TIMEOUT and finish (every access stays inside the arrays). The
+    context stays usable: after a zero fill the next call is exact."""
+    import time
+    cfg = ei.WORKLOADS[4].scaled(N=2048)          # a dozen CTAs
+    idx, _ = ei.make_routing(cfg, 51)
+    ref = oracle.layout(idx, cfg.E, cfg.R)
+    ws = torch.zeros(ep.ep_layout_workspace_bytes(cfg.N, cfg.K, cfg.E, cfg.R), dtype=torch.uint8, device="cuda")
+    lay = ep.new_layout(to_dev(idx), cfg.E, cfg.R)
+    ws[:4] = 0xFF
+    st = _status()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    ep.ep_get_dispatch_layout(lay, ws, st)
+    val = status_value(st)
+    waited = time.perf_counter() - t0
+    assert val & ep.EP_ST_TIMEOUT and val & ep.EP_ST_WORKSPACE, val
+    assert 0.5 < waited < 30.0, waited
+    ws.zero_()
     st = _status()
     ep.ep_get_dispatch_layout(lay, ws, st)
     _layout_equal(lay, ref)
@@ -363,54 +392,6 @@ def test_combine_masked_and_capacity():
     assert status_value(st) & ep.EP_ST_CAPACITY
 
 
-# ------------------------------------------------------- full-size samples ----
-@pytest.mark.parametrize("c", [3, 4, 5])
-def test_full_size_sampled(c):
-    cfg = ei.WORKLOADS[c]
-    d = ei.make_inputs(cfg, seed=0)
-    st = _status()
-    x = to_dev_bf16(d["x"])
-    w = to_dev(d["topk_weights"])
-    lay = ep.get_dispatch_layout(to_dev(d["topk_idx"]), cfg.E, cfg.R, status=st)
-    ref_lay = oracle.layout(d["topk_idx"], cfg.E, cfg.R)
-    _layout_equal(lay, ref_lay)
-    res = ep.dispatch(x, lay, w, use_fp8=cfg.fp8, status=st)
-    out = ep.combine(res.expert_x if not cfg.fp8 else
-                     ep.dispatch(x, lay, w, with_rank=False).expert_x, lay, w, status=st)
-    assert status_value(st) == 0
-    # sampled tokens, checked one by one against the oracle
-    rng = np.random.default_rng(c)
-    toks = np.unique(np.concatenate([[0, cfg.N - 1], rng.integers(0, cfg.N, 64)]))
-    sub_x = d["x"][toks]
-    if cfg.fp8:
-        q, s = oracle.quantize_rows(sub_x)
-    es = ref_lay["expert_slot"][toks]
-    rs = ref_lay["rank_slot"][toks]
-    gx = res.expert_x
-    for i, t in enumerate(toks):
-        for k in range(cfg.K):
-            row = es[i, k]
-            if row < 0:
-                continue
-            if cfg.fp8:
-                assert np.array_equal(u8(gx[row]), q[i])
-                assert np.array_equal(res.expert_scales[row].cpu().numpy(), s[i])
-            else:
-                assert np.array_equal(u16(gx[row]), sub_x[i])
-            assert int(res.expert_src[row]) == t * cfg.K + k
-        for r in range(cfg.R):
-            row = rs[i, r]
-            if row >= 0:
-                assert int(res.rank_src[row]) == t
-                want = q[i] if cfg.fp8 else sub_x[i]
-                got = u8(res.rank_x[row]) if cfg.fp8 else u16(res.rank_x[row])
-                assert np.array_equal(got, want)
-    # combine on the sampled tokens: identity experts over the BF16 rows
-    y_rows = u16(ep.dispatch(x, lay, w, with_rank=False).expert_x) if cfg.fp8 else u16(res.expert_x)
-    ref_out, _ = oracle.combine(y_rows, ref_lay["expert_slot"][toks], d["topk_weights"][toks])
-    assert np.array_equal(u16(out[toks]), ref_out)
-
-
 # ------------------------------------------------------------ low latency ----
 @pytest.mark.parametrize("c,n_s,H,T", [(1, 16, 7168, 16), (1, 5, 256, 128), (2, 16, 512, 128),
                                        (2, 128, 1024, 128)])
@@ -452,51 +433,6 @@ def test_ll_dispatch_parity(c, n_s, H, T):
     got = u16(out)
     assert bf16_ulp_diff(got, ref_out).max() <= 1
     assert np.array_equal(got, ref_out)
-    assert status_value(st) == 0
-
-
-@pytest.mark.parametrize("c", [1, 2])
-def test_ll_full_size(c):
-    cfg = ei.WORKLOADS[c]
-    d = ei.make_inputs(cfg, seed=0)
-    st = _status()
-    x = to_dev_bf16(d["x"])
-    recv, cnt, handle, hook = ep.low_latency_dispatch(x, to_dev(d["topk_idx"]), cfg.T, cfg.E, cfg.R,
-                                                      use_fp8=cfg.fp8, status=st)
-    hook()
-    ref_lay = oracle.layout(d["topk_idx"], cfg.E, cfg.R)
-    cnt = cnt.cpu().numpy()
-    assert np.array_equal(cnt, ref_lay["num_tokens_per_expert"])
-    rx, rs = recv if cfg.fp8 else (recv, None)
-    src = handle.recv_src.cpu().numpy()
-    n_s = cfg.N // cfg.R
-    if cfg.fp8:
-        q, s = oracle.quantize_rows(d["x"])
-    for e in sorted(set([0, cfg.E - 1]) | set(range(3, cfg.E, 17))):
-        toks = np.nonzero((d["topk_idx"] == e).any(1))[0]
-        assert np.array_equal(src[e, :cnt[e]], toks)
-        if cfg.fp8:
-            assert np.array_equal(u8(rx[e, :cnt[e]]), q[toks])
-            assert np.array_equal(rs[e, :cnt[e]].cpu().numpy(), s[toks])
-        else:
-            assert np.array_equal(u16(rx[e, :cnt[e]]), d["x"][toks])
-        cnt_s = np.bincount(toks // n_s, minlength=cfg.R)
-        rng_ = handle.layout_range[e].cpu().numpy()
-        assert np.array_equal(rng_ & 0xFFFFFFFF, cnt_s)
-    # combine over BF16 copies of the received rows (identity experts): out ~ x
-    if cfg.fp8:
-        y = torch.zeros((cfg.E, cfg.R * cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
-        r2, _, h2, hook2 = ep.low_latency_dispatch(x, to_dev(d["topk_idx"]), cfg.T, cfg.E, cfg.R,
-                                                   use_fp8=False)
-        hook2()
-        y, handle = r2, h2
-    else:
-        y = rx
-    out = ep.low_latency_combine(y, to_dev(d["topk_weights"]), handle, status=st)
-    xf = oracle.f32_from_bf16(d["x"]).astype(np.float64)
-    of = oracle.f32_from_bf16(u16(out)).astype(np.float64)
-    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(xf), 2.0 ** -126))) - 7)
-    assert np.all(np.abs(of - xf) <= ulp)
     assert status_value(st) == 0
 
 
