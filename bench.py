@@ -21,6 +21,11 @@ region (pipelined: a step's copies overlap its neighbours' compute).
 
 --impl reference times the CPU oracle (plain single-threaded C++) on the same
 workload, each step a bounded sample of tokens.
+
+The default run (the large prefill workload, no variant flags) also measures
+workloads 1, 2, 3 and 5 the same way and reports them under `workloads`.
+`cpu_baseline` is the oracle on every host core, with its single-core figure
+beside it.
 """
 from __future__ import annotations
 
@@ -44,7 +49,9 @@ import epinputs as ei  # noqa: E402
 METRIC = "dispatch+combine tokens/s and HBM GB/s (% of GB300 peak) at 1 GPU"
 DEFAULT_WORKLOAD = 4          # the 16384-token large prefill workload
 L2_FLUSH_BYTES = 256 << 20
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dispatch_kernel_prefill_large.md")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dispatch_traffic.json")
+NOMINAL_HBM_GBS = 8000.0      # GB300's ~8 TB/s nominal HBM3e bandwidth (context beside the measured peak)
+EXTRA_WORKLOADS = (1, 2, 3, 5)  # measured in the default run beside the headline workload
 KERNEL_SOURCES = [os.path.join(ROOT, "combine_ep_get_dispatch_gb300", "csrc", f)
                   for f in ("dispatch.cu", "common.cuh", "kernels.cuh")]
 
@@ -77,7 +84,27 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--l2-flush", default="write", choices=["write", "write-read"],
+                    help="between steps: write 256 MiB (default), or write it and read it back so that no "
+                         "dirty line of the flush is left in L2 when the step starts")
+    ap.add_argument("--extra-workloads", default="auto",
+                    help="workloads measured beside the headline one and reported under `workloads` "
+                         "(comma-separated, 'none', or 'auto': 1,2,3,5 for the default run)")
     return ap.parse_args()
+
+
+def extra_workloads(args):
+    """The other workloads measured in this run (the default run: all four)."""
+    if args.extra_workloads == "none":
+        return []
+    if args.extra_workloads != "auto":
+        return [int(v) for v in args.extra_workloads.split(",") if v]
+    default_variant = (args.fp8_scales == "fp32" and args.expert_alignment == 1 and not args.combine_bias
+                       and args.combine == "flat" and not args.training and args.ll_combine == "one-phase"
+                       and not args.mask_ranks and not args.fused_layout and not args.graph)
+    if args.workload == DEFAULT_WORKLOAD and args.tokens is None and default_variant:
+        return list(EXTRA_WORKLOADS)
+    return []
 
 
 def peaks():
@@ -96,16 +123,12 @@ def kernel_hash() -> str:
 
 
 def profile_traffic():
-    """(bytes per full-size dispatch launch, source hash) from the committed ncu summary."""
+    """(DRAM bytes per full-size dispatch launch, source hash) from the committed
+    ncu figures (profiles/dispatch_traffic.json), or (None, None)."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None, None
-    traffic = src = None
-    for line in open(PROFILE_TRAFFIC):
-        if line.startswith("traffic_bytes_per_full_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
-        if line.startswith("kernel_source_sha256_16:"):
-            src = line.split(":", 1)[1].strip()
-    return traffic, src
+    d = json.load(open(PROFILE_TRAFFIC))
+    return d.get("dram_bytes_per_full_launch"), d.get("kernel_source_sha256_16")
 
 
 class ClockSampler:
@@ -118,7 +141,6 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -133,12 +155,6 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def mark(self, begin: bool):
-        if begin:
-            self.t0 = time.time()
-        else:
-            self.t1 = time.time()
-
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -147,7 +163,8 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0, t1):
+        """Median SM clock, maximum clock and throttle reasons seen between t0 and t1 (host time)."""
         rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -159,7 +176,7 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        inside = [r for r in rows if self.t0 and self.t1 and self.t0 - 0.06 <= r[0] <= self.t1 + 0.06] or rows
+        inside = [r for r in rows if t0 and t1 and t0 - 0.06 <= r[0] <= t1 + 0.06] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for r in inside:
@@ -260,6 +277,14 @@ class NormalWorkload:
                              "layout+dispatch": f"layout_kernel + {dk} (programmatic dependent pair)",
                              "combine": "combine_kernel", "combine_to_ranks": "combine_to_ranks_kernel",
                              "combine_ranks": "combine_kernel"}
+
+    def launches_per_step(self):
+        """This library's kernel launches in one step."""
+        n = 2                                    # layout, dispatch (one call or two)
+        n += 1 if self.align > 1 else 0          # zero fill of the padding rows
+        n += 2 if self.two_level else 1          # combine
+        n += 2 if self.training else 0           # combine backward, dispatch backward
+        return n
 
     def layout_for(self, idx):
         L = self.lay
@@ -373,9 +398,20 @@ class LLWorkload:
         else:
             self.phases = ["send", "recv", "combine"]
         self.dominant = "send"
-        self.kernel_names = {"send": "layout_kernel<ll> + dispatch_kernel", "recv": "ll_recv_kernel",
+        small = cfg.N > 0 and cfg.N * cfg.K <= 4096 and cfg.E * cfg.R <= 16384
+        self.kernel_names = {"send": "ll_send_small_kernel" if small else "layout_kernel<ll> + dispatch_kernel",
+                             "recv": "ll_recv_kernel",
                              "combine": "combine_kernel", "combine_send": "combine_kernel<gather>",
                              "combine_recv": "combine_kernel"}
+
+    def launches_per_step(self):
+        """This library's kernel launches in one step: the send is one launch
+        for a batch of at most 4096 (token, slot) entries with E * R <= 16384
+        (the library's one-launch send), else two; then the receive and the
+        combine (two launches when two-phase)."""
+        c = self.cfg
+        send = 1 if (c.N > 0 and c.N * c.K <= 4096 and c.E * c.R <= 16384) else 2
+        return send + 1 + (2 if self.two_phase else 1)
 
     def layout_for(self, idx):
         return idx
@@ -431,7 +467,8 @@ def workload_config(cfg, args, world, rows):
             "ranks": cfg.R, "max_tokens_per_rank": cfg.T,
             "dispatch_dtype": (f"fp8_e4m3 + {args.fp8_scales} scales / 128 ch" if cfg.fp8 else "bf16"),
             "combine_dtype": "bf16 (fp32 accumulation)",
-            "l2": "flushed between steps (256 MiB write)",
+            "l2": ("flushed between steps (256 MiB write)" if args.l2_flush == "write" else
+                   "flushed between steps (256 MiB write, then read back: no dirty flush lines left)"),
             "variant": {"expert_alignment": args.expert_alignment, "combine_bias": args.combine_bias,
                         "combine": args.combine, "ll_combine": args.ll_combine,
                         "fp8_scales": args.fp8_scales, "training": args.training,
@@ -458,38 +495,44 @@ def oracle_rows(cfg, args):
     return r
 
 
-def run_ours(args):
-    import torch
+def build_workload(cfg, args, dev, headline):
+    """The workload object of cfg; variant flags apply to the headline workload only."""
     import combine_ep_get_dispatch_gb300 as ep
-
-    rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    cfg = ei.WORKLOADS[args.workload]
-    if args.tokens:
-        cfg = cfg.scaled(N=args.tokens)
     inp = ei.make_inputs(cfg, seed=0)
     if cfg.mode == "ll":
+        if not headline:
+            return LLWorkload(cfg, dev, inp)
         wl = LLWorkload(cfg, dev, inp, two_phase=args.ll_combine == "two-phase", scales=args.fp8_scales,
                         bias=args.combine_bias)
         for r in (int(v) for v in args.mask_ranks.split(",") if v):
             ep.low_latency_update_mask_buffer(wl.ws, r, num_ranks=cfg.R)   # shrink mode: rank r is out
-    else:
-        wl = NormalWorkload(cfg, dev, inp, scales=args.fp8_scales, align=args.expert_alignment,
-                            bias=args.combine_bias, two_level=args.combine == "two-level", training=args.training,
-                            fused=args.fused_layout)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    lay = wl.layout_for(wl.idx)
+        return wl
+    if not headline:
+        return NormalWorkload(cfg, dev, inp)
+    return NormalWorkload(cfg, dev, inp, scales=args.fp8_scales, align=args.expert_alignment,
+                          bias=args.combine_bias, two_level=args.combine == "two-level", training=args.training,
+                          fused=args.fused_layout)
 
-    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    sampler.start()
-    time.sleep(0.3)
+
+def flush_l2(flush, i, mode):
+    """Evict the last step's data from L2: write 256 MiB (twice L2); with
+    mode write-read, also read it back so the dirty lines of the fill are
+    written back before the step starts."""
+    import torch
+    flush.fill_(i & 0xFF)
+    if mode == "write-read":
+        flush.view(torch.int64).max()
+
+
+def time_workload(wl, cfg, args, dev, world, stream, flush, sampler, with_e2e, with_graph):
+    """Warm-up, then `steps` timed steps (L2 flushed before each, CUDA events
+    around every phase on the launching stream); optionally the graph replay
+    and the pipelined end-to-end run. Returns the raw timings."""
+    import torch
+    import combine_ep_get_dispatch_gb300 as ep
+    lay = wl.layout_for(wl.idx)
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2(flush, 1, args.l2_flush)
         wl.run(stream, wl.x, lay, wl.w)
     torch.cuda.synchronize()
     if world > 1:
@@ -497,26 +540,26 @@ def run_ours(args):
     nph = len(wl.phases)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     torch.cuda.synchronize()
-    sampler.mark(True)
+    t_begin = time.time()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)   # write 256 MiB between steps: nothing of the last step stays in L2
+        flush_l2(flush, i, args.l2_flush)   # nothing of the last step stays in L2
         wl.run(stream, wl.x, lay, wl.w, evs[i])
     torch.cuda.synchronize()
-    sampler.mark(False)
+    t_end = time.time()
     if world > 1:
         torch.distributed.barrier()
     phase_ms = {ph: np.array([e[j].elapsed_time(e[j + 1]) for e in evs]) for j, ph in enumerate(wl.phases)}
     step_ms = np.array([e[0].elapsed_time(e[nph]) for e in evs])
-    total_ms = float(step_ms.sum())
     st = int(wl.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {ep.ep_error_string(st)}")
+    out = {"phase_ms": phase_ms, "total_ms": float(step_ms.sum()), "window": (t_begin, t_end), "graph_ms": None,
+           "e2e": None}
 
     # The same step captured once in a CUDA graph and replayed K times (the
     # launches of a step then cost one graph launch); L2 flushed before each
     # replay, CUDA events around it. Reported beside the eager numbers.
-    graph = None
-    if args.graph:
+    if with_graph:
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -529,15 +572,12 @@ def run_ours(args):
         gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i, args.l2_flush)
             gev[i][0].record(stream)
             g.replay()
             gev[i][1].record(stream)
         torch.cuda.synchronize()
-        g_ms = float(np.mean([a.elapsed_time(b) for a, b in gev]))
-        g_ms = max_over_ranks([g_ms], dev, world)[0]
-        graph = {"ms_per_step": round(g_ms, 4), "value": round(job_throughput(cfg.N, world, g_ms), 1),
-                 "unit": "tokens/s"}
+        out["graph_ms"] = float(np.mean([a.elapsed_time(b) for a, b in gev]))
         st = int(wl.status.item())
         if st != 0:
             raise RuntimeError(f"device status {st}: {ep.ep_error_string(st)}")
@@ -546,8 +586,7 @@ def run_ours(args):
     # serving loop runs it: while step i computes, step i+1's inputs go up on
     # one stream and step i-1's output comes down on another (two sets of
     # device inputs and outputs; events order the reuse of each set).
-    e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         xp, ip, wp = wl.x_host.pin_memory(), wl.idx_host.pin_memory(), wl.w_host.pin_memory()
         outp = [torch.empty(wl.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         xd = [torch.empty_like(wl.x) for _ in range(2)]
@@ -594,29 +633,81 @@ def run_ours(args):
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
         if not torch.equal(outp[(n_all - 1) & 1], wl.out.cpu()):
             raise RuntimeError("e2e output differs from the device-resident run")
-        e2e = (e2e_ms, xp.numel() * 2 + ip.numel() * 4 + wp.numel() * 4, outp[0].numel() * 2)
-    sampler.stop()
+        out["e2e"] = (e2e_ms, xp.numel() * 2 + ip.numel() * 4 + wp.numel() * 4, outp[0].numel() * 2)
+    return out
 
-    total_ms, e2e_ms_max = max_over_ranks([total_ms, e2e[0] if e2e else 0.0], dev, world)
-    if rank != 0:
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return
 
-    peak, peak_kind = peaks()
+def phase_report(wl, timing, ms_per_step, peak, peak_kind):
+    """Per-phase µs, algorithmic GB/s and fractions of the measured and the nominal HBM peak."""
     nbytes = wl.algorithmic_bytes()
-    mean_s = {ph: float(v.mean()) / 1e3 for ph, v in phase_ms.items()}
-    ms_per_step = total_ms / args.steps
-    N = cfg.N
-    value = job_throughput(N, world, ms_per_step)
+    mean_s = {ph: float(v.mean()) / 1e3 for ph, v in timing["phase_ms"].items()}
     phases = {}
     for ph in wl.phases:
         gbs = nbytes[ph] / mean_s[ph] / 1e9
         phases[f"{ph}_us"] = round(mean_s[ph] * 1e6, 2)
         phases[f"{ph}_gbs"] = round(gbs, 1)
         phases[f"{ph}_frac"] = round(gbs / peak, 4)
+        phases[f"{ph}_frac_nominal"] = round(gbs / NOMINAL_HBM_GBS, 4)
     phases["step_gbs"] = round(sum(nbytes.values()) / (ms_per_step / 1e3) / 1e9, 1)
-    phases["peak_note"] = f"fractions of the {peak_kind} HBM copy peak {peak} GB/s"
+    phases["peak_note"] = (f"*_frac: fractions of the {peak_kind} HBM copy peak {peak} GB/s; "
+                           f"*_frac_nominal: of the {NOMINAL_HBM_GBS:.0f} GB/s nominal peak")
+    return phases, nbytes, mean_s
+
+
+def run_ours(args):
+    import torch
+    import combine_ep_get_dispatch_gb300 as ep  # noqa: F401  (fails loudly if the library is missing)
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = ei.WORKLOADS[args.workload]
+    if args.tokens:
+        cfg = cfg.scaled(N=args.tokens)
+    wl = build_workload(cfg, args, dev, headline=True)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    time.sleep(0.3)
+    timing = time_workload(wl, cfg, args, dev, world, stream, flush, sampler, not args.no_e2e, args.graph)
+
+    # The other workloads, measured the same way (same steps, warm-up, L2
+    # flush and events), reported under `workloads`.
+    extras = {}
+    for w in extra_workloads(args):
+        if w == args.workload:
+            continue
+        c2 = ei.WORKLOADS[w]
+        wl2 = build_workload(c2, args, dev, headline=False)
+        t2 = time_workload(wl2, c2, args, dev, world, stream, flush, sampler, not args.no_e2e, False)
+        extras[w] = (c2, wl2.rows(), wl2, t2)
+        del wl2
+        torch.cuda.empty_cache()
+    sampler.stop()
+
+    total_ms = timing["total_ms"]
+    e2e = timing["e2e"]
+    vals = max_over_ranks([total_ms, e2e[0] if e2e else 0.0, timing["graph_ms"] or 0.0]
+                          + [t[3]["total_ms"] for t in extras.values()]
+                          + [t[3]["e2e"][0] if t[3]["e2e"] else 0.0 for t in extras.values()], dev, world)
+    total_ms, e2e_ms_max, graph_ms = vals[0], vals[1], vals[2]
+    extra_tot = dict(zip(extras, vals[3:3 + len(extras)]))
+    extra_e2e = dict(zip(extras, vals[3 + len(extras):]))
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    ms_per_step = total_ms / args.steps
+    N = cfg.N
+    value = job_throughput(N, world, ms_per_step)
+    phases, nbytes, mean_s = phase_report(wl, timing, ms_per_step, peak, peak_kind)
     dom = wl.dominant
     achieved = nbytes[dom] / mean_s[dom] / 1e9
     traffic = None
@@ -640,18 +731,38 @@ def run_ours(args):
                 "see epinputs for the grouped and Zipf recipes)",
         "config": workload_config(cfg, args, world, wl.rows()),
         "phases": phases,
-        **({"graph": graph} if graph else {}),
         "roofline": {"bound": "hbm", "kernel": wl.kernel_names[dom], "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind},
-        "gpu_launches": (len(wl.phases) + (1 if cfg.mode == "ll" else 0) + (1 if getattr(wl, "fused", False) else 0)
-                         + (1 if getattr(wl, "align", 1) > 1 else 0)) * args.steps,
-        "clocks": sampler.summary(),
+                     "algorithmic_bytes": nbytes[dom], "peak_kind": peak_kind,
+                     "peak_nominal": NOMINAL_HBM_GBS, "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "gpu_launches": wl.launches_per_step() * args.steps,
+        "clocks": sampler.summary(*timing["window"]),
     }
+    if timing["graph_ms"] is not None:
+        line["graph"] = {"ms_per_step": round(graph_ms, 4), "value": round(job_throughput(N, world, graph_ms), 1),
+                         "unit": "tokens/s"}
     if e2e:
         line["e2e"] = {"value": round(job_throughput(N, world, e2e_ms_max), 1), "unit": "tokens/s",
                        "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
                        "ms_per_step": round(e2e_ms_max, 4)}
+    if extras:
+        line["workloads"] = {}
+        for w, (c2, rows2, wl2, t2) in extras.items():
+            ms2 = extra_tot[w] / args.steps
+            ph2, nb2, ms_s2 = phase_report(wl2, t2, ms2, peak, peak_kind)
+            d2 = wl2.dominant
+            ach2 = nb2[d2] / ms_s2[d2] / 1e9
+            entry = {"workload": c2.name, "value": round(job_throughput(c2.N, world, ms2), 1), "unit": "tokens/s",
+                     "ms_per_step": round(ms2, 4), "phases": ph2,
+                     "dominant": {"phase": d2, "kernel": wl2.kernel_names[d2], "achieved": round(ach2, 1),
+                                  "frac": round(ach2 / peak, 4), "frac_nominal": round(ach2 / NOMINAL_HBM_GBS, 4)},
+                     "rows": rows2, "gpu_launches": wl2.launches_per_step() * args.steps,
+                     "clocks": sampler.summary(*t2["window"])}
+            if t2["e2e"]:
+                entry["e2e"] = {"value": round(job_throughput(c2.N, world, extra_e2e[w]), 1), "unit": "tokens/s",
+                                "h2d_bytes_per_step": t2["e2e"][1], "d2h_bytes_per_step": t2["e2e"][2],
+                                "ms_per_step": round(extra_e2e[w], 4)}
+            line["workloads"][c2.name] = entry
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_sample_tokens)
     print(json.dumps(line), flush=True)
@@ -685,20 +796,41 @@ def _sample(cfg, n_tok):
     return d
 
 
-def cpu_baseline(cfg, n_tok):
-    """The oracle as written (single thread) on the first n_tok tokens of the workload."""
-    sub = _sample(cfg, n_tok)
-    n_tok = sub["n_tok"]
+def _time_oracle(sub, budget_s=10.0, max_reps=20):
     _oracle_step(sub)  # warm the library and the page cache
     reps, t = 0, 0.0
-    while t < 10.0 and reps < 20:
+    while t < budget_s and reps < max_reps:
         t0 = time.perf_counter()
         _oracle_step(sub)
         t += time.perf_counter() - t0
         reps += 1
-    return {"value": round(n_tok * reps / t, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_tok} of {cfg.N} tokens of {cfg.name} (the whole step on those tokens), "
-                      f"{reps} reps, {t:.1f} s"}
+    return reps, t
+
+
+def cpu_baseline(cfg, n_tok):
+    """The oracle on the first n_tok tokens of the workload (the whole step on
+    those tokens), on every host core (its OpenMP build: the row loops of
+    dispatch and combine in parallel, the layout sequential, identical
+    results), with the plain single-threaded build's figure beside it."""
+    import oracle
+    sub = _sample(cfg, n_tok)
+    n_tok = sub["n_tok"]
+    oracle.use_all_cores(False)
+    reps1, t1 = _time_oracle(sub)
+    one = {"value": round(n_tok * reps1 / t1, 1), "unit": "tokens/s", "cores": 1,
+           "sample": f"{n_tok} of {cfg.N} tokens, {reps1} reps, {t1:.1f} s"}
+    if not oracle.use_all_cores(True):
+        return {**one, "kind": "oracle", "sample": f"{n_tok} of {cfg.N} tokens of {cfg.name} (the whole step on "
+                                                     f"those tokens), {reps1} reps, {t1:.1f} s; no OpenMP build"}
+    try:
+        cores = oracle.threads()
+        reps, t = _time_oracle(sub)
+    finally:
+        oracle.use_all_cores(False)
+    return {"value": round(n_tok * reps / t, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_tok} of {cfg.N} tokens of {cfg.name} (the whole step on those tokens: layout "
+                      f"sequential, row loops of dispatch and combine on {cores} threads), {reps} reps, {t:.1f} s",
+            "single_core": one}
 
 
 def run_reference(args):

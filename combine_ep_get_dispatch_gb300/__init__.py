@@ -123,6 +123,7 @@ def lib() -> ctypes.CDLL:
         "ep_ll_dispatch_recv": (I, [P, SZ, I, I, I, I, I, P, P, P, P, P]),
         "ep_ll_combine": (I, [P, P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_fp8_e4m3_encode": (I, [P, P, I64, P]),
+        "ep_fp8_quantize": (I, [P, I64, I, I, P, P, P]),
         "ep_ll_combine_send": (I, [P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_ll_combine_recv": (I, [P, P, P, P, SZ, I, I, I, I, I, I, P, P, P]),
         "ep_ll_update_mask": (I, [P, SZ, I, I, I, P]),
@@ -350,6 +351,12 @@ def ep_ll_clean_mask(workspace, R, stream=None) -> None:
 
 def ep_fp8_e4m3_encode(x: torch.Tensor, out: torch.Tensor, stream=None) -> None:
     _check(lib().ep_fp8_e4m3_encode(_p(x), _p(out), x.numel(), _stream(stream)), "ep_fp8_e4m3_encode")
+
+
+def ep_fp8_quantize(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, fp8: int = EP_FP8, stream=None) -> None:
+    """x [rows, H] bf16 -> q [rows, H] uint8 (E4M3) and scales [rows, H/128] (fp32, or uint8 UE8M0)."""
+    _check(lib().ep_fp8_quantize(_p(x), x.shape[0], x.shape[1], int(fp8), _p(q), _p(scales), _stream(stream)),
+           "ep_fp8_quantize")
 
 
 # -------------------------------------------------------------- page-level ----

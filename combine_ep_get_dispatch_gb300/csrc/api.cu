@@ -400,9 +400,36 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int N, int K, in
   const LLWs w = ll_ws(N, K, E, R);
   if (!workspace || workspace_bytes < w.total) return EP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return EP_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // Without the layout kernel when the routing table is small enough: a
+  // small batch in one launch (each block derives its slots from the whole
+  // routing table, one block publishes counts, ranges and header), a larger
+  // one by a per-source histogram kernel and its dependent row kernel.
+  if (ll_send_form(N, K, E, R) != LLSendForm::kLayout) {
+    LLSendParams sp{};
+    sp.x = static_cast<const uint16_t*>(x);
+    sp.idx = topk_idx;
+    sp.N = N; sp.K = K; sp.H = H; sp.E = E; sp.R = R; sp.L = E / R;
+    sp.ns = N / R;
+    sp.cap = static_cast<int64_t>(R) * T;
+    sp.fp8_flags = fp8_flags;
+    sp.recv_x = static_cast<uint8_t*>(recv_x);
+    sp.recv_scales = use_fp8 ? recv_scales : nullptr;
+    sp.recv_src = recv_src;
+    sp.count = at<int32_t>(workspace, w.count);
+    sp.range = at<int64_t>(workspace, w.range);
+    sp.slot_map = at<int32_t>(workspace, w.slot);
+    sp.hdr = at<LLHeader>(workspace, w.hdr);
+    sp.hdr_value = LLHeader{kMagicSent, N, K, E, R, T, H, use_fp8, 0};
+    sp.rank_mask = at<int32_t>(workspace, w.mask);
+    sp.hist = at<int32_t>(workspace, w.chunk);  // [R, E]: the chunk-count area
+    sp.status = status;
+    return cuda_rc(launch_ll_send(sp, s));
+  }
+
   const int gmax = layout_max_ctas(E, R, false);
   if (gmax < 1 || R > gmax) return EP_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // A small batch runs the layout as one CTA with a group of g warps per
   // source rank (no grid barrier, no exchange of chunk counts through
@@ -567,6 +594,16 @@ int ep_ll_query_mask(const void* workspace, size_t workspace_bytes, int num_rank
 
 int ep_ll_clean_mask(void* workspace, size_t workspace_bytes, int num_ranks, void* stream) {
   return ll_mask_call(workspace, workspace_bytes, num_ranks, 2, 0, 0, nullptr, stream);
+}
+
+int ep_fp8_quantize(const void* x, int64_t rows, int hidden, int fp8_flags, uint8_t* q, void* scales,
+                    void* stream) {
+  if (!flags_ok(fp8_flags) || !(fp8_flags & EP_FP8) || !hidden_ok(hidden, fp8_flags) || rows < 0)
+    return EP_ERR_INVALID_ARG;
+  if (rows > 0 && (!x || !q || !scales)) return EP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q)) return EP_ERR_ALIGNMENT;
+  return cuda_rc(launch_quantize_rows(static_cast<const uint16_t*>(x), rows, hidden, fp8_flags, q, scales,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 int ep_fp8_e4m3_encode(const float* in, uint8_t* out, int64_t n, void* stream) {

@@ -136,11 +136,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
 // shared memory with one bulk TMA load (the whole row in flight at once); the
 // warps then quantise it in place, 512 channels per warp per step: lanes own
 // 16 consecutive channels (8 lanes = one 128-channel block), take the block's
-// max by shuffles, divide by the scale (IEEE) and convert to E4M3, writing the
-// codes over the front of the staged row. Each destination row then leaves by
-// one bulk store (cp.async.bulk shared->global), and the scales follow with
-// plain stores (a UE8M0 scale row is not a multiple of 16 bytes). At 14.9 KB
-// of shared memory per token about 14 tokens are in flight per SM.
+// max by shuffles, divide by the scale (correctly rounded) and convert to
+// E4M3, writing the codes over the front of the staged row. As soon as a
+// step's 2048 channels are quantised they leave by one bulk store
+// (cp.async.bulk shared->global) per destination row, while the next step is
+// quantised; the scales follow with plain stores (a UE8M0 scale row is not a
+// multiple of 16 bytes). Launched with at most 120 KB of staged rows per SM
+// (8 tokens of hidden 7168): every first-wave block loads its row at once, so
+// the cap shortens the read burst and the synchronous quantisation before the
+// first stores (measured on GB300: the 4096-token hidden-7168 dispatch went
+// from 85 to 79 us with the three changes; the PM-sampled DRAM timeline had
+// shown ~8 us without traffic between the first wave's loads and its stores).
 // Measured on GB300 (all bit-identical): the row loaded through registers one
 // step ahead (each token then waits out ~14 load latencies behind the write
 // traffic); a separate E4M3 row (fewer tokens in flight); one warp per token
@@ -148,6 +154,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
 // kernel's ramp and tail are too: four warps took the 4096-token FP8
 // dispatches from 90.1 to 86.0 us and 79.9 to 74.2 us).
 constexpr int kF8Warps = 4;                  // warps per token (one token per block)
+constexpr size_t kF8StagedBytesPerSM = 120 * 1024;  // see launch_fp8
+constexpr size_t kSmemPerSM = 228 * 1024;            // shared memory of one SM
+constexpr size_t kSmemReservedPerBlock = 1024;       // the runtime's share of it per block
 constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank copies
 
 // Smallest power of two >= s for s >= 0 (exact on the bit pattern; a
@@ -189,8 +198,30 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
   if ((flags & (EP_FP8_ROUND_SCALE | EP_FP8_UE8M0)) && sc > 0.0f) sc = pow2_ceil(sc);
   if ((flags & EP_FP8_UE8M0) && m > 0.0f) sc = fmaxf(sc, __uint_as_float(0x00400000u));  // 2^-127
   if (sc > 0.0f) {
+    if (sc >= 0x1p-92f && sc <= 0x1p126f) {
+      // x / s, correctly rounded, from one correctly rounded reciprocal
+      // y = 1/s per block: q0 = x * y is within an ulp of x / s, the
+      // remainder x - s * q0 is exact by a fused multiply-add, and
+      // q0 + remainder * y rounds to x / s (Markstein's correction step,
+      // "Computation of elementary functions on the IBM RISC System/6000
+      // processor", IBM J. Res. Dev. 34(1), 1990). A zero remainder keeps q0
+      // itself, so -0 / s stays -0. The remainder is exact only if it does
+      // not underflow: for |x / s| >= 2^-11 (below that every E4M3 code is
+      // a zero) it is a multiple of 2^(e_s - 57), which s >= 2^-92 keeps at
+      // or above 2^-149; s <= 2^126 keeps y normal. Smaller or larger scales
+      // take the IEEE division. A device test compares every (x, amax) pair
+      // of BF16 inputs with the oracle's IEEE division.
+      const float y = __frcp_rn(sc);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
+      for (int i = 0; i < 16; ++i) {
+        const float q0 = f[i] * y;
+        const float r = fmaf(-sc, q0, f[i]);
+        f[i] = r == 0.0f ? q0 : fmaf(r, y, q0);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
+    }
   }
   uint4 q;
   q.x = e4m3x4(f[0], f[1], f[2], f[3]);
@@ -320,6 +351,7 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
   // Step c0 covers channels [c0, c0 + 512 * kF8Warps), 512 per warp. Its codes
   // go to bytes [c0, c0 + 512 * kF8Warps) of the row, which later steps never
   // read; the barrier keeps them from overwriting this step's own inputs.
+  int seg_lo = 0;
   for (int c0 = 0; c0 < H; c0 += 512 * kF8Warps) {
     const int c = c0 + w * 512 + lane * 16;
     uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
@@ -333,6 +365,18 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
     if (c < H) {
       *reinterpret_cast<uint4*>(row + c) = q;
       if ((lane & 7) == 0) scales[c >> 7] = sc;
+    }
+    const int hi = c0 + 512 * kF8Warps;
+    if (!kLateDest && hi < H) {
+      fence_proxy_async_smem();
+      __syncthreads();
+      const int n = s_n, ne = s_ne;
+      for (int d = tid; d < n; d += kF8Warps * 32) {
+        uint8_t* base = d < ne ? p.exp_x : p.rank_x;
+        bulk_s2g(base + static_cast<int64_t>(drow[d]) * H + seg_lo, row + seg_lo, static_cast<unsigned>(hi - seg_lo));
+      }
+      bulk_commit();
+      seg_lo = hi;
     }
   }
   if (kLateDest && w == 0) {
@@ -350,7 +394,7 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
   // One bulk store per destination row, spread over the block's threads.
   for (int d = tid; d < n; d += kF8Warps * 32) {
     uint8_t* base = d < ne ? p.exp_x : p.rank_x;
-    bulk_s2g(base + static_cast<int64_t>(drow[d]) * H, row, static_cast<unsigned>(H));
+    bulk_s2g(base + static_cast<int64_t>(drow[d]) * H + seg_lo, row + seg_lo, static_cast<unsigned>(H - seg_lo));
   }
   bulk_commit();
   const bool ue8m0 = p.fp8_flags & EP_FP8_UE8M0;
@@ -368,11 +412,374 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
   bulk_wait_read<0>();
 }
 
-// Launch `fn` with one DispatchParams argument; with `pdl`, as the dependent
+// ---- low-latency send without the layout kernel ------------------------------------
+// The layout kernel of the general send computes every slot with a grid-wide
+// scan and costs a decode-sized batch ~15 us before any row can leave. The
+// slot of (token t, slot k) routed to expert e is
+//   j = pre[e][s] + #{(t', k') before (t, k) in source rank s = t / ns,
+//                     routed to e},
+// where pre[e][s] counts e's entries from the source ranks before s. Two
+// forms compute it without the layout:
+//   small batch (N * K <= 4096, E * R <= 16384): one launch. Block 0 (the
+//     table block) counts the routed entries per (expert, source rank) in
+//     shared memory and publishes the per-expert counts, the per-(expert,
+//     source) ranges and the header that the receive phase and the combine
+//     read; every other block counts the entries of all earlier tokens itself
+//     (a few KB, from L2), so it needs nothing from the table block.
+//   larger batch (N * K <= 65536, E * R <= 16384, a source rank's entries
+//     <= 8192): two launches. A histogram kernel, one block per source rank,
+//     counts that source's routed entries per expert (hist[s][e]); the row
+//     kernel is its programmatic dependent: its blocks start at once, count
+//     the earlier entries of their own source rank, bring in (and quantise)
+//     their rows, and only then wait for the histograms and add pre[e][s] =
+//     sum over s' < s of hist[s'][e] for their own experts; its block 0
+//     publishes the counts, ranges and header from the histograms.
+// A row block copies span sp of token t's row: one bulk TMA load in, FP8
+// quantisation in place, one bulk store per slot to row e * cap + j of the
+// fixed receive buffer. Shrink mode: entries of masked ranks (the expert's, or
+// the token's source) are dropped, exactly as in the layout of the general
+// send; so are indices outside [-1, E) (flagged by the table).
+constexpr int kLLRowThreads = 128;
+constexpr int kLLHistThreads = 256;  // the histogram kernel of the larger form
+constexpr int kLLSmallBlocksPerSM = 2;
+constexpr int kLLMaxRanks = 128;  // E * R <= kLLSmallMaxTable with R <= E gives R <= 128
+
+// n / d by a multiply-high with magic = ceil(2^32 / d) (magic 0 stands for
+// d == 1): exact whenever n * d <= 2^32 (n, d >= 0).
+__device__ __forceinline__ int div_magic(int n, uint32_t magic) {
+  return magic ? static_cast<int>(__umulhi(static_cast<unsigned>(n), magic)) : n;
+}
+
+// Entries idx[i0 + j] for j < n, thread tid taking j = tid, tid + NT, ...,
+// kBatch loads in flight per thread before any of them is used (a store to
+// shared memory or a shared atomic between two loads would otherwise keep the
+// next load from being issued early: the pointers may alias).
+template <int kBatch, typename F>
+__device__ __forceinline__ void for_entries(const int32_t* idx, int i0, int n, int tid, int NT, F&& use) {
+  for (int b = tid; b < n; b += kBatch * NT) {
+    int v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = b + u * NT;
+      v[u] = j < n ? __ldg(idx + i0 + j) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = b + u * NT;
+      if (j < n) use(j, v[u]);
+    }
+  }
+}
+
+// The table of the small form (all threads of the block): counts per
+// (expert, source rank) from the routing table, then per-expert counts, the
+// per-(expert, source) ranges and the header. hist: shared memory of
+// E * (R + 1) + E ints (a row of R + 1 per expert, so the scan over source
+// ranks, one thread per expert, is free of bank conflicts).
+__device__ void ll_table(const LLSendParams& p, int32_t* hist) {
+  __shared__ int s_mask[kLLMaxRanks];
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int K = p.K, E = p.E, R = p.R, RP = R + 1;
+  int32_t* tot = hist + E * RP;  // [E]
+  const int NK = p.N * K;
+  const int m = (tid < R && p.rank_mask) ? __ldg(p.rank_mask + tid) : 0;
+  if (tid < R) s_mask[tid] = m;
+  for (int i = tid; i < E * RP; i += NT) hist[i] = 0;
+  const bool any_masked = __syncthreads_or(m != 0);
+  bool bad = false;
+  for_entries<16>(p.idx, 0, NK, tid, NT, [&](int i, int e) {
+    if (e == -1) return;
+    if (e < 0 || e >= E) {
+      bad = true;
+      return;
+    }
+    const int src = div_magic(i, p.magic_nsK);
+    if (any_masked && (s_mask[src] != 0 || s_mask[div_magic(e, p.magic_L)] != 0)) return;
+    atomicAdd(&hist[e * RP + src], 1);
+  });
+  if (__syncthreads_or(bad) && tid == 0) flag(p.status, EP_ST_BAD_INDEX);
+  for (int e = tid; e < E; e += NT) {
+    int off = 0;
+    for (int s = 0; s < R; ++s) {
+      const int c = hist[e * RP + s];
+      hist[e * RP + s] = off;
+      off += c;
+    }
+    tot[e] = off;
+    p.count[e] = off;
+  }
+  __syncthreads();
+  // Rows j >= cap overflow the region (only repeated experts in a row can
+  // get there): a range covers the rows that landed.
+  for (int i = tid; i < E * R; i += NT) {
+    const int e = div_magic(i, p.magic_R), s = i - e * R;
+    const int off = hist[e * RP + s];
+    const int64_t lo = min(static_cast<int64_t>(off), p.cap);
+    const int64_t hi = min(static_cast<int64_t>(s + 1 < R ? hist[e * RP + s + 1] : tot[e]), p.cap);
+    p.range[i] = (lo << 32) | (hi - lo);
+  }
+  if (tid == 0) *p.hdr = p.hdr_value;
+}
+
+// The same counts, ranges and header for the larger form, from the
+// per-source histograms p.hist [R, E]: a thread per expert runs the prefix
+// over source ranks, eight counts loaded at a time.
+__device__ void ll_table_from_hist(const LLSendParams& p) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int E = p.E, R = p.R;
+  for (int e = tid; e < E; e += NT) {
+    int off = 0;
+    for (int s0 = 0; s0 < R; s0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = s0 + u < R ? __ldcg(p.hist + static_cast<int64_t>(s0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (s0 + u >= R) break;
+        const int64_t lo = min(static_cast<int64_t>(off), p.cap);
+        const int64_t hi = min(static_cast<int64_t>(off) + c[u], p.cap);
+        p.range[static_cast<int64_t>(e) * R + s0 + u] = (lo << 32) | (hi - lo);
+        off += c[u];
+      }
+    }
+    p.count[e] = off;
+  }
+  if (tid == 0) *p.hdr = p.hdr_value;
+}
+
+// The larger form's histogram of source rank s = blockIdx.x: hist[s][e] =
+// routed entries of that source for expert e (entries of masked ranks
+// dropped; indices outside [-1, E) flagged). hist: shared memory of E ints.
+__device__ void ll_source_hist(const LLSendParams& p, int32_t* hist) {
+  __shared__ int s_mask[kLLMaxRanks];
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int E = p.E, R = p.R, s = blockIdx.x, nsK = p.ns * p.K;
+  const int m = (tid < R && p.rank_mask) ? __ldg(p.rank_mask + tid) : 0;
+  if (tid < R) s_mask[tid] = m;
+  for (int e = tid; e < E; e += NT) hist[e] = 0;
+  const bool any_masked = __syncthreads_or(m != 0);
+  const bool src_masked = any_masked && s_mask[s] != 0;
+  bool bad = false;
+  for_entries<8>(p.idx, s * nsK, nsK, tid, NT, [&](int, int e) {
+    if (e == -1) return;
+    if (e < 0 || e >= E) {
+      bad = true;
+      return;
+    }
+    if (src_masked || (any_masked && s_mask[div_magic(e, p.magic_L)] != 0)) return;
+    atomicAdd(&hist[e], 1);
+  });
+  if (__syncthreads_or(bad) && tid == 0) flag(p.status, EP_ST_BAD_INDEX);
+  for (int e = tid; e < E; e += NT) p.hist[static_cast<int64_t>(s) * E + e] = hist[e];
+}
+
+// Span sp of token t's row (all kLLRowThreads threads of the block). kMid:
+// the larger form (count within the own source rank, then wait for the table
+// kernel and add its prefix); otherwise the small form (count over every
+// earlier token).
+template <bool kFp8, int KMAX, bool kMid>
+__device__ void ll_row(const LLSendParams& p, int t, int sp, uint8_t* smem) {
+  __shared__ int s_e[KMAX], s_cnt[KMAX];
+  __shared__ int32_t s_row[KMAX];
+  __shared__ int s_mask[kLLMaxRanks];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, NT = kLLRowThreads;
+  const int K = p.K, E = p.E, R = p.R;
+  const int c0 = sp * p.span, c1 = min(p.H, c0 + p.span);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* row = smem + kBarBytes;
+  float* scales = reinterpret_cast<float*>(row + round_up(static_cast<unsigned>(p.span) * 2u, 128u));
+  int32_t* s_ent = reinterpret_cast<int32_t*>(scales + p.span / 128);  // the counted entries
+  const unsigned in_bytes = static_cast<unsigned>(c1 - c0) * 2u;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, in_bytes);
+    bulk_g2s(row, p.x + static_cast<int64_t>(t) * p.H + c0, in_bytes, bar);
+  }
+  // Every load this block needs goes out together: the entries to count
+  // (staged in shared memory), the token's own slots and the rank mask.
+  const int src_t = t / p.ns;
+  const int tK = t * K;
+  const int i0 = kMid ? src_t * p.ns * K : 0;  // first entry counted
+  for_entries<8>(p.idx, i0, tK - i0, tid, NT, [&](int j, int v) { s_ent[j] = v; });
+  if (tid < K) {
+    s_e[tid] = __ldg(p.idx + tK + tid);
+    s_cnt[tid] = 0;
+  }
+  const int m = (tid < R && p.rank_mask) ? __ldg(p.rank_mask + tid) : 0;
+  if (tid < R) s_mask[tid] = m;
+  // Publishes the mbarrier's initialisation (every thread waits on it
+  // below), the entries, the slots' experts and the mask.
+  const bool any_masked = __syncthreads_or(m != 0);
+  const bool src_masked = any_masked && s_mask[src_t] != 0;
+  int key[KMAX], cnt[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    const int e = k < K ? s_e[k] : -1;
+    const bool ok = e >= 0 && e < E && !(any_masked && (src_masked || s_mask[div_magic(e, p.magic_L)] != 0));
+    key[k] = ok ? e : -1;
+    cnt[k] = 0;
+  }
+  // Earlier entries from unmasked source ranks that name each key.
+  for (int i = i0 + tid; i < tK; i += NT) {
+    const int x = s_ent[i - i0];
+    if (x < 0) continue;
+    if (!kMid && any_masked && s_mask[div_magic(i, p.magic_nsK)] != 0) continue;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) cnt[k] += (x == key[k]) ? 1 : 0;
+  }
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    if (k >= K) break;
+    const int c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt[k])));
+    if (lane == 0 && c) atomicAdd(&s_cnt[k], c);
+  }
+  // Every thread sees the span land itself (it reads it); the block leaves
+  // together if any thread's bounded wait gave up, after the load in flight
+  // has landed (bounded). The barrier also publishes the counts.
+  const bool ok = mbar_wait(bar, 0, p.status);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) mbar_drain(bar, 0);
+    __syncthreads();
+    return;
+  }
+  const int n = c1 - c0;
+  if (kFp8) {
+    // In place, as in dispatch_fp8_kernel: a step reads 512 channels per warp
+    // into registers, the block barrier, then the codes go over bytes that
+    // no later step reads.
+    for (int q0 = 0; q0 < n; q0 += 512 * (kLLRowThreads / 32)) {
+      const int c = q0 + w * 512 + lane * 16;
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (c < n) {
+        v0 = *reinterpret_cast<const uint4*>(row + 2 * c);
+        v1 = *reinterpret_cast<const uint4*>(row + 2 * c + 16);
+      }
+      __syncthreads();
+      float sc;
+      const uint4 q = quantize16(v0, v1, sc, p.fp8_flags);
+      if (c < n) {
+        *reinterpret_cast<uint4*>(row + c) = q;
+        if ((lane & 7) == 0) scales[c >> 7] = sc;
+      }
+    }
+  }
+  // The larger form: the histograms' sum over the earlier source ranks for
+  // each of the token's experts, pairs (k, s') spread over the block.
+  __shared__ int s_pre[KMAX];
+  if (kMid) {
+    if (tid < K) s_pre[tid] = 0;
+    grid_dependency_wait();
+    __syncthreads();
+    const int KS = K * src_t;
+    for (int q0 = tid; q0 < KS; q0 += 4 * NT) {
+      int c[4], kk[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + u * NT;
+        c[u] = 0;
+        kk[u] = 0;
+        if (q < KS) {
+          const int k = q / src_t, s2 = q - k * src_t;
+          const int e = s_e[k];
+          kk[u] = k;
+          if (e >= 0 && e < E) c[u] = __ldcg(p.hist + static_cast<int64_t>(s2) * E + e);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c[u]) atomicAdd(&s_pre[kk[u]], c[u]);
+    }
+    __syncthreads();
+  }
+  if (tid < K) {
+    const int e0 = s_e[tid];
+    const bool ok0 = e0 >= 0 && e0 < E && !(any_masked && (src_masked || s_mask[div_magic(e0, p.magic_L)] != 0));
+    const int e = ok0 ? e0 : -1;
+    int32_t r = -1;
+    if (e >= 0) {
+      // The token's own earlier slots naming the same expert (a slot equal
+      // to a valid key is valid itself).
+      int j = s_cnt[tid] + (kMid ? s_pre[tid] : 0);
+      for (int k2 = 0; k2 < tid; ++k2) j += (s_e[k2] == e) ? 1 : 0;
+      if (j < p.cap)
+        r = static_cast<int32_t>(static_cast<int64_t>(e) * p.cap + j);
+      else
+        flag(p.status, EP_ST_LL_OVERFLOW);
+    }
+    s_row[tid] = r;
+    if (sp == 0) {
+      p.slot_map[tK + tid] = r;
+      if (r >= 0 && p.recv_src) p.recv_src[r] = t;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  const int eb = kFp8 ? 1 : 2;
+  for (int k = tid; k < K; k += NT) {
+    const int32_t r = s_row[k];
+    if (r >= 0)
+      bulk_s2g(p.recv_x + (static_cast<int64_t>(r) * p.H + c0) * eb, row, static_cast<unsigned>(n * eb));
+  }
+  bulk_commit();
+  if (kFp8 && p.recv_scales) {
+    const int nsc = n / 128, b0 = c0 / 128, nall = p.H / 128;
+    const bool ue8m0 = p.fp8_flags & EP_FP8_UE8M0;
+    for (int i = tid; i < K * nsc; i += NT) {
+      const int k = i / nsc, bb = i - k * nsc;
+      const int32_t r = s_row[k];
+      if (r < 0) continue;
+      const int64_t at = static_cast<int64_t>(r) * nall + b0 + bb;
+      if (ue8m0)
+        static_cast<uint8_t*>(p.recv_scales)[at] = ue8m0_byte(scales[bb]);
+      else
+        static_cast<float*>(p.recv_scales)[at] = scales[bb];
+    }
+  }
+  // The shared span must outlive the stores' reads of it.
+  bulk_wait_read<0>();
+}
+
+// The small form: block 0 is the table, block 1 + t * nsplit + sp a row span.
+template <bool kFp8, int KMAX>
+__global__ void __launch_bounds__(kLLRowThreads) ll_send_small_kernel(const LLSendParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (blockIdx.x == 0) {
+    ll_table(p, reinterpret_cast<int32_t*>(smem));
+    return;
+  }
+  const int b = blockIdx.x - 1;
+  ll_row<kFp8, KMAX, false>(p, b / p.nsplit, b % p.nsplit, smem);
+}
+
+// The larger form: the histogram kernel (one block per source rank) releases
+// its dependent row kernel at once.
+__global__ void __launch_bounds__(kLLHistThreads) ll_hist_kernel(const LLSendParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  launch_dependents();
+  ll_source_hist(p, reinterpret_cast<int32_t*>(smem));
+}
+
+// Block 0 publishes counts, ranges and header once the histograms are in;
+// block 1 + t * nsplit + sp is a row span.
+template <bool kFp8, int KMAX>
+__global__ void __launch_bounds__(kLLRowThreads) ll_send_rows_kernel(const LLSendParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  if (blockIdx.x == 0) {
+    grid_dependency_wait();
+    ll_table_from_hist(p);
+    return;
+  }
+  const int b = blockIdx.x - 1;
+  ll_row<kFp8, KMAX, true>(p, b / p.nsplit, b % p.nsplit, smem);
+}
+
+// Launch `fn` with one parameter block; with `pdl`, as the dependent
 // of a programmatic pair (it may start before the kernel ahead of it on the
 // stream completes, and waits for that kernel in-kernel).
-cudaError_t launch_ex(void (*fn)(DispatchParams), unsigned grid, unsigned threads, size_t smem, cudaStream_t s,
-                      bool pdl, const DispatchParams& p) {
+template <typename Params>
+cudaError_t launch_ex(void (*fn)(Params), unsigned grid, unsigned threads, size_t smem, cudaStream_t s, bool pdl,
+                      const Params& p) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -391,7 +798,16 @@ cudaError_t launch_ex(void (*fn)(DispatchParams), unsigned grid, unsigned thread
 // to the freed slots.
 cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s, bool pdl) {
   if (p.N <= 0) return cudaSuccess;
-  const size_t smem = kBarBytes + f8_warp_bytes(p.H);
+  // At most kF8StagedBytesPerSM of staged rows per SM: every block of the
+  // first wave loads its row at once, so this caps the first wave's read
+  // burst (and its synchronous quantisation) before the first stores; the
+  // request for more shared memory than a block needs is what caps it.
+  size_t smem = kBarBytes + f8_warp_bytes(p.H);
+  const size_t blocks = kF8StagedBytesPerSM / smem;
+  if (blocks >= 1 && blocks < kSmemPerSM / (smem + kSmemReservedPerBlock)) {
+    const size_t capped = kSmemPerSM / blocks - kSmemReservedPerBlock;
+    if (capped > smem) smem = capped;
+  }
   void (*fn)(DispatchParams) = pdl ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
   if (err != cudaSuccess) return err;
@@ -418,7 +834,72 @@ cudaError_t launch_bf16(const DispatchParams& p, cudaStream_t s, bool pdl) {
   return launch_ex(fn, static_cast<unsigned>(grid), W * 32, smem, s, pdl, p);
 }
 
+template <bool kFp8, int KMAX>
+cudaError_t launch_ll_rows_variant(const LLSendParams& p, unsigned grid, size_t smem, cudaStream_t s, bool mid) {
+  if (!mid) {
+    void (*fn)(LLSendParams) = ll_send_small_kernel<kFp8, KMAX>;
+    const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
+    if (err != cudaSuccess) return err;
+    fn<<<grid, kLLRowThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  }
+  void (*fn)(LLSendParams) = ll_send_rows_kernel<kFp8, KMAX>;
+  const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
+  if (err != cudaSuccess) return err;
+  return launch_ex(fn, grid, kLLRowThreads, smem, s, /*pdl=*/true, p);
+}
+
 }  // namespace
+
+LLSendForm ll_send_form(int N, int K, int E, int R) {
+  if (N <= 0 || static_cast<int64_t>(E) * R > kLLSmallMaxTable) return LLSendForm::kLayout;
+  const int64_t NK = static_cast<int64_t>(N) * K;
+  if (NK <= kLLSmallMaxEntries) return LLSendForm::kSmall;
+  if (NK <= kLLMidMaxEntries && static_cast<int64_t>(N / R) * K <= kLLMidMaxSourceEntries) return LLSendForm::kMid;
+  return LLSendForm::kLayout;
+}
+
+// Blocks per token: about kLLSmallBlocksPerSM blocks per SM over the batch,
+// each a span of whole 16-byte BF16 groups (8 channels) or, for FP8, whole
+// 128-channel scale blocks. p.hist: the [R, E] per-source histograms of the
+// larger form (workspace).
+cudaError_t launch_ll_send(LLSendParams p, cudaStream_t s) {
+  const LLSendForm form = ll_send_form(p.N, p.K, p.E, p.R);
+  if (form == LLSendForm::kLayout) return cudaErrorInvalidValue;
+  const bool mid = form == LLSendForm::kMid;
+  const bool fp8 = p.fp8_flags & EP_FP8;
+  const int sms = device_sms(current_device());
+  const int gran = fp8 ? 128 : 8;
+  const int units = p.H / gran;
+  int nsplit = (kLLSmallBlocksPerSM * sms + p.N - 1) / p.N;
+  nsplit = nsplit < 1 ? 1 : (nsplit > units ? units : nsplit);
+  const int span_units = (units + nsplit - 1) / nsplit;
+  p.span = span_units * gran;
+  p.nsplit = (units + span_units - 1) / span_units;
+  auto magic = [](int d) { return d > 1 ? static_cast<uint32_t>(((uint64_t(1) << 32) + d - 1) / d) : 0u; };
+  p.magic_nsK = magic(p.ns * p.K);
+  p.magic_L = magic(p.L);
+  p.magic_R = magic(p.R);
+  // Row block: the staged span, its FP8 scales, the entries it counts.
+  const size_t counted = mid ? static_cast<size_t>(p.ns) * p.K : static_cast<size_t>(p.N) * p.K;
+  const size_t row_smem = kBarBytes + round_up(static_cast<unsigned>(p.span) * 2u, 128u) +
+                          static_cast<size_t>(p.span / 128) * 4u + sizeof(int32_t) * counted;
+  const size_t table_smem = sizeof(int32_t) * (static_cast<size_t>(p.E) * (p.R + 1) + p.E);
+  if (mid) {
+    if (!p.hist) return cudaErrorInvalidValue;
+    ll_hist_kernel<<<p.R, kLLHistThreads, sizeof(int32_t) * p.E, s>>>(p);
+    const cudaError_t lerr = cudaGetLastError();
+    if (lerr != cudaSuccess) return lerr;
+  }
+  // Block 0 of the larger form's row kernel needs no shared table.
+  const size_t smem = mid ? row_smem : (row_smem > table_smem ? row_smem : table_smem);
+  const unsigned grid = 1u + static_cast<unsigned>(p.N) * static_cast<unsigned>(p.nsplit);
+  if (p.K <= 8)
+    return fp8 ? launch_ll_rows_variant<true, 8>(p, grid, smem, s, mid)
+               : launch_ll_rows_variant<false, 8>(p, grid, smem, s, mid);
+  return fp8 ? launch_ll_rows_variant<true, EP_MAX_TOPK>(p, grid, smem, s, mid)
+             : launch_ll_rows_variant<false, EP_MAX_TOPK>(p, grid, smem, s, mid);
+}
 
 // Zero the padding rows of an aligned expert-major buffer: rows
 // [expert_off[e] + count[e], expert_off[e+1]) of each expert e (payload,
@@ -449,6 +930,49 @@ __global__ void __launch_bounds__(256) pad_zero_kernel(const PadParams p) {
 cudaError_t launch_pad_zero(const PadParams& p, cudaStream_t s) {
   if (p.E <= 0) return cudaSuccess;
   pad_zero_kernel<<<dim3(p.E, kPadSlices), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Rows to E4M3 + scales with the dispatch's quantiser: a warp per 512
+// channels of a row, lanes owning 16 channels (8 lanes per scale block).
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ x, int64_t rows, int H,
+                                                            int flags, uint8_t* __restrict__ q, void* scales) {
+  const int lane = threadIdx.x & 31;
+  const int per_row = (H + 511) / 512;
+  const int64_t nw = rows * per_row;
+  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const bool ue8m0 = flags & EP_FP8_UE8M0;
+  for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < nw; wi += stride) {
+    const int64_t r = wi / per_row;
+    const int c = static_cast<int>(wi - r * per_row) * 512 + lane * 16;
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+    if (c < H) {
+      v0 = __ldg(reinterpret_cast<const uint4*>(x + r * H + c));
+      v1 = __ldg(reinterpret_cast<const uint4*>(x + r * H + c + 8));
+    }
+    float sc;
+    const uint4 qq = quantize16(v0, v1, sc, flags);
+    if (c < H) {
+      *reinterpret_cast<uint4*>(q + r * H + c) = qq;
+      if ((lane & 7) == 0) {
+        const int64_t at = r * (H / 128) + (c >> 7);
+        if (ue8m0)
+          static_cast<uint8_t*>(scales)[at] = ue8m0_byte(sc);
+        else
+          static_cast<float*>(scales)[at] = sc;
+      }
+    }
+  }
+}
+
+cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int H, int fp8_flags, uint8_t* q, void* scales,
+                                 cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int64_t warps = rows * ((H + 511) / 512);
+  const int64_t cap = static_cast<int64_t>(device_sms(current_device())) * 64;
+  const int64_t blocks = (warps + 7) / 8;
+  quantize_rows_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, s>>>(x, rows, H, fp8_flags, q,
+                                                                                          scales);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,31 @@ struct DispatchParams {
   int32_t* status;
 };
 
+// The low-latency send without the layout kernel (ll_send_small_kernel, or
+// ll_hist_kernel + ll_send_rows_kernel).
+struct LLSendParams {
+  const uint16_t* x;          // [N, H] BF16
+  const int32_t* idx;         // [N, K]
+  int N, K, H, E, R, L;
+  int ns;                     // tokens per source rank (N / R)
+  int64_t cap;                // R * T rows per expert region
+  int fp8_flags;              // 0: BF16 rows; EP_FP8 (+ scale format flags)
+  uint8_t* recv_x;            // [E, cap, H] BF16 words or E4M3 bytes
+  void* recv_scales;          // [E, cap, H/128] fp32 or UE8M0 bytes (FP8), or null
+  int32_t* recv_src;          // [E, cap] or null
+  int32_t* count;             // [E] workspace: rows routed to each expert
+  int64_t* range;             // [E, R] workspace: (offset << 32) | count per source rank
+  int32_t* slot_map;          // [N, K] workspace: e * cap + j, or -1
+  LLHeader* hdr;
+  LLHeader hdr_value;
+  const int32_t* rank_mask;   // [R] shrink mode, non-zero = masked
+  int nsplit;                 // blocks per token, each one span of the row
+  int span;                   // channels per span
+  uint32_t magic_nsK, magic_L, magic_R;  // ceil(2^32 / d) for d = ns * K, L, R (0 when d == 1)
+  int32_t* hist;              // [R, E] workspace: routed entries per (source rank, expert) (larger form)
+  int32_t* status;
+};
+
 struct CombineParams {
   const uint16_t* y;     // [y_rows, H] BF16
   int64_t y_rows;
@@ -168,8 +193,22 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_combine_to_ranks(const CombineRanksParams& p, cudaStream_t s);
 cudaError_t launch_combine_backward(const CombineBwdParams& p, cudaStream_t s);
 cudaError_t launch_pad_zero(const PadParams& p, cudaStream_t s);
+// Forms of the low-latency send (ll_send_form): one launch for a small batch
+// (N * K <= kLLSmallMaxEntries); a per-source histogram kernel and its
+// dependent row kernel for a larger one (N * K <= kLLMidMaxEntries, (N / R) * K <=
+// kLLMidMaxSourceEntries); both need E * R <= kLLSmallMaxTable. Otherwise
+// the routing layout kernel and the dispatch kernel.
+constexpr int kLLSmallMaxEntries = 4096;
+constexpr int kLLSmallMaxTable = 16384;
+constexpr int kLLMidMaxEntries = 65536;
+constexpr int kLLMidMaxSourceEntries = 8192;
+enum class LLSendForm { kSmall, kMid, kLayout };
+LLSendForm ll_send_form(int N, int K, int E, int R);
+cudaError_t launch_ll_send(LLSendParams p, cudaStream_t s);  // kSmall or kMid
 cudaError_t launch_ll_mask(int32_t* mask, int R, int mode, int rank, int value, int32_t* out, cudaStream_t s);
 cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s);
 cudaError_t launch_e4m3_encode(const float* in, uint8_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_quantize_rows(const uint16_t* x, int64_t rows, int H, int fp8_flags, uint8_t* q, void* scales,
+                                 cudaStream_t s);
 
 }  // namespace ep

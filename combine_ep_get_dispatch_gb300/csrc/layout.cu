@@ -248,9 +248,9 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
         // up to the end of its last warp).
         const int g = p.ll_src_warps;
         const int last = __shfl_sync(0xffffffffu, incl[j], min(lane + g - 1, 31));
-        const int pre = incl[j] - v[j];
-        if (lane < W && lane % g == 0)
-          p.ll_range[static_cast<int64_t>(col) * R + lane / g] = (static_cast<int64_t>(pre) << 32) | (last - pre);
+        const int64_t lo = min(static_cast<int64_t>(incl[j] - v[j]), p.ll_cap);
+        const int64_t hi = min(static_cast<int64_t>(last), p.ll_cap);
+        if (lane < W && lane % g == 0) p.ll_range[static_cast<int64_t>(col) * R + lane / g] = (lo << 32) | (hi - lo);
       }
       if (lane < W) hist[lane * CP + col] = incl[j] - v[j];
       if (lane == 31) {
@@ -361,9 +361,13 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   if (kLL) {
     // Chunks are source ranks here: (offset << 32) | count of expert e's rows
     // from source `cta` (the one-CTA form wrote its ranges in the column scan).
-    for (int e = tid; !warp_src && e < E; e += NT)
-      p.ll_range[static_cast<int64_t>(e) * R + cta] =
-          (static_cast<int64_t>(base[e]) << 32) | static_cast<int64_t>(own[e]);
+    // Rows at j >= ll_cap overflow the region (only repeated experts in a
+    // row get there); a range covers the rows that landed.
+    for (int e = tid; !warp_src && e < E; e += NT) {
+      const int64_t lo = min(static_cast<int64_t>(base[e]), p.ll_cap);
+      const int64_t hi = min(static_cast<int64_t>(base[e]) + own[e], p.ll_cap);
+      p.ll_range[static_cast<int64_t>(e) * R + cta] = (lo << 32) | (hi - lo);
+    }
     if (cta == 0 && tid == 0) *p.ll_hdr = p.hdr_value;
   }
   // Running counters: warp prefix + chunk prefix (+ global offset in normal mode).

@@ -383,11 +383,15 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *   status       EP_ST_BAD_INDEX, EP_ST_TIMEOUT and EP_ST_WORKSPACE as for
  *                the layout
  * Slots of ranks masked in the workspace (shrink mode, ep_ll_update_mask)
- * are dropped. Enqueues two launches: the routing layout, then the row
- * copies as its programmatic dependent (they load and quantise their rows
- * while the layout runs, and wait for it in-kernel before reading a slot).
- * The rows are in place when the stream reaches the end of this call; the
- * counts are published by ep_ll_dispatch_recv.
+ * are dropped. A small batch (N * K <= 4096 and E * R <= 16384) is one
+ * launch: every block finds the slots of its own token from the whole
+ * routing table, one block writes the counts and ranges. A larger batch is
+ * two launches: the routing layout, then the row copies as its programmatic
+ * dependent (they load and quantise their rows while the layout runs, and
+ * wait for it in-kernel before reading a slot); the second may fail with
+ * EP_ERR_CUDA after the first was enqueued. The rows are in place when the
+ * stream reaches the end of this call; the counts are published by
+ * ep_ll_dispatch_recv.
  */
 int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, int num_topk,
                         int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
@@ -397,13 +401,19 @@ int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, 
 /*
  * Low-latency dispatch, receive phase: the deferred second launch (the
  * "hook"). Publishes the per-expert receive counts and, per (expert, source
- * rank), the range of rows that came from that source.
+ * rank), the range of rows that came from that source. ("How DeepEP enables
+ * hook-based overlapping", "Two-Phase Kernel Architecture": the receive phase
+ * is a separate launch that runs when the hook is called; "DeepEP V1
+ * (legacy) guide", section 6.3: the hook guarantees the rows have arrived and
+ * returns recv_count, the tokens each local expert received.)
  *
  *   workspace     the workspace a send filled (same sizes)
  *   recv_count    [E] int32: rows received by each expert
  *   layout_range  [E, R] int64: (offset << 32) | count of the rows of expert
  *                 e that came from source rank s (offsets are an exclusive
- *                 scan over s); may be NULL
+ *                 scan over s; only rows inside the expert's R*T region are
+ *                 counted, so with EP_ST_LL_OVERFLOW the ranges cover the
+ *                 rows that landed); may be NULL
  *   cumulative_recv_stats  [E] int32 or NULL: each call adds recv_count to it
  *                 (the per-expert load statistics of "DeepEP V1 (legacy)
  *                 guide", section 6.3, cumulative_local_expert_recv_stats;
@@ -510,6 +520,26 @@ int ep_ll_clean_mask(void* workspace, size_t workspace_bytes, int num_ranks, voi
  * pointers.
  */
 int ep_fp8_e4m3_encode(const float* in, uint8_t* out, int64_t n, void* stream);
+
+/*
+ * FP8 quantisation of BF16 rows, exactly as the FP8 dispatch quantises a
+ * token's row before copying it ("DeepEP V1 (legacy) guide", sections 5.2(6)
+ * and 6.3: E4M3 data with one fp32 scale per 128 channels; round_scale,
+ * use_ue8m0): per row and 128-channel block b, s_b = amax_b / 448 (fp32,
+ * nearest; raised to the next power of two with EP_FP8_ROUND_SCALE or
+ * EP_FP8_UE8M0, and kept >= 2^-127 with EP_FP8_UE8M0), q = e4m3(x / s_b) with
+ * a correctly rounded division, rounded to nearest even and saturated to
+ * +-448; an all-zero block has s = 0 and q = e4m3(x).
+ *
+ *   x          [rows, hidden] BF16, 16-byte aligned
+ *   rows       >= 0
+ *   hidden     a multiple of 128, <= EP_MAX_HIDDEN
+ *   fp8_flags  EP_FP8, optionally with EP_FP8_ROUND_SCALE or EP_FP8_UE8M0
+ *   q          [rows, hidden] E4M3 bytes, 16-byte aligned
+ *   scales     [rows, hidden/128] fp32, or UE8M0 bytes with EP_FP8_UE8M0
+ */
+int ep_fp8_quantize(const void* x, int64_t rows, int hidden, int fp8_flags, uint8_t* q, void* scales,
+                    void* stream);
 
 #ifdef __cplusplus
 }

@@ -38,10 +38,11 @@
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -shared -fPIC.
 // The only fused multiply-add is the explicit std::fmaf of the combine.
 // A second build of this same file with -fopenmp (libep_oracle_omp.so) runs
-// the per-token row loops of dispatch and combine, and the per-expert loop of
-// the low-latency dispatch, on every host core: those iterations write
-// disjoint rows, so the results are identical; the layout stays sequential.
-// It exists only to time the oracle on all cores next to the plain build.
+// the per-token row loops of dispatch and combine, the per-expert loop of the
+// low-latency dispatch and the per-row loop of quantize_rows on every host
+// core: those iterations write disjoint rows, so the results are identical;
+// the layout stays sequential. It exists to time the oracle on all cores next
+// to the plain build and to run the large exhaustive quantisation check.
 
 #include <cmath>
 #include <cstdint>
@@ -212,6 +213,8 @@ void oracle_e4m3_from_f32_n(const float* in, uint8_t* out, int64_t n) {
 // rows x H BF16 -> rows x H E4M3 and rows x H/128 fp32 scales (flags: kFp8
 // plus optional kRoundScale / kUe8m0).
 void oracle_quantize_rows(const uint16_t* x, int64_t rows, int H, uint8_t* q, float* scales, int flags) {
+  // Rows are independent: split over threads in the all-core build.
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r)
     quantize_row(x + r * H, H, q + r * H, scales + r * (H / 128), flags | kFp8);
 }

@@ -436,6 +436,52 @@ def test_ll_dispatch_parity(c, n_s, H, T):
     assert status_value(st) == 0
 
 
+@pytest.mark.parametrize("E,R,n_s,K", [
+    (4, 2, 2, 4),        # 16 entries: the one-launch send
+    (1024, 32, 4, 8),    # E * R above the one-launch table: one-CTA layout + dispatch
+    (4, 2, 600, 4),      # 4800 entries: the multi-CTA layout + dispatch
+])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_ll_masked_bad_repeated_and_overflow(E, R, n_s, K, fp8):
+    """Every low-latency send path against the oracle on a routing with masked
+    slots, out-of-range indices and repeated experts, the first half of the
+    tokens sending two slots each to expert 0 so that its region (R * T rows)
+    overflows: counts, ranges (rows that landed), rows, scales, sources,
+    status bits, and the combine (overflowed slots are skipped)."""
+    N, H, T = R * n_s, 256, n_s
+    idx = _rand_idx(N, K, E, seed=E + n_s + K, p_mask=0.15, distinct=False)
+    idx[: N // 2 + 1, 0:2] = 0
+    idx[1::5, K - 1] = E
+    idx[2::7, K - 2] = -9
+    x = ei.make_x(N, H, seed=n_s)
+    w = ei.uniform01(ei.stream_key(n_s, 1), N * K).reshape(N, K).astype(np.float32)
+    st = _status()
+    recv, cnt, handle, hook = ep.low_latency_dispatch(to_dev_bf16(x), to_dev(idx), T, E, R, use_fp8=fp8, status=st)
+    hook()
+    ref = oracle.ll_dispatch(x, idx, E, R, T, fp8)
+    assert ref["status"] == oracle.BAD_INDEX | oracle.LL_OVERFLOW
+    assert status_value(st) == ep.EP_ST_BAD_INDEX | ep.EP_ST_LL_OVERFLOW
+    cnt = cnt.cpu().numpy()
+    assert np.array_equal(cnt, ref["recv_count"])
+    assert np.array_equal(handle.layout_range.cpu().numpy(), ref["layout_range"])
+    landed = np.minimum(cnt, R * T)
+    rx, rs = recv if fp8 else (recv, None)
+    gx = u8(rx) if fp8 else u16(rx)
+    src = handle.recv_src.cpu().numpy()
+    for e in range(E):
+        n = landed[e]
+        assert np.array_equal(gx[e, :n], ref["recv_x"][e, :n]), e
+        assert np.array_equal(src[e, :n], ref["recv_src"][e, :n]), e
+        if fp8:
+            assert np.array_equal(rs[e, :n].cpu().numpy(), ref["recv_scales"][e, :n]), e
+    y = _expert_outputs(E * R * T, H, seed=E).reshape(E, R * T, H)
+    st = _status()
+    out = ep.low_latency_combine(to_dev_bf16(y), to_dev(w), handle, status=st)
+    ref_out, _ = oracle.ll_combine(y, ref["slot_map"], w)
+    assert np.array_equal(u16(out), ref_out)
+    assert status_value(st) == 0
+
+
 def test_ll_receive_without_send_and_mismatch():
     cfg = ei.WORKLOADS[1].scaled(H=256)
     N, K, E, R, T = cfg.N, cfg.K, cfg.E, cfg.R, cfg.T
