@@ -54,6 +54,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
   int32_t* s_row = s_dyn;
   float* s_w = reinterpret_cast<float*>(s_dyn + K);
   int32_t* s_k = s_dyn + 2 * K;
+  // Launched as a programmatic dependent: nothing is touched before the
+  // kernel ahead of it on the stream has completed.
+  grid_dependency_wait();
   if (p.ll_hdr) {
     if (tid == 0) {
       const LLHeader h = *p.ll_hdr;
@@ -168,11 +171,8 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t cap = int64_t(1) << 30;
   const int grid = static_cast<int>(items < cap ? items : cap);
   const size_t smem = static_cast<size_t>(p.K) * 12;
-  if (p.gather)
-    combine_kernel<true><<<grid, kThreads, smem, s>>>(p, nchunk);
-  else
-    combine_kernel<false><<<grid, kThreads, smem, s>>>(p, nchunk);
-  return cudaGetLastError();
+  return launch_kernel(p.gather ? combine_kernel<true> : combine_kernel<false>, dim3(grid), dim3(kThreads), smem, s,
+                       /*dependent=*/true, p, nchunk);
 }
 
 // ---- two-level combine, first level --------------------------------------------

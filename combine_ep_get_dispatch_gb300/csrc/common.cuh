@@ -157,6 +157,27 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Launch `fn` on stream s. With `dependent`, as a programmatic dependent of
+// the kernel before it on the stream: it may be scheduled while that kernel
+// drains, so its launch latency hides behind that kernel's tail, and it must
+// call grid_dependency_wait() before it touches any memory (which makes it
+// ordered exactly as a plain launch would be).
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool dependent,
+                          Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fn, static_cast<Args&&>(args)...);
+}
+
 // ---- grid-wide barrier (cooperative launches only) --------------------------
 // One barrier per launch over two words that persist across launches: bar[0]
 // counts arrivals and is zero between launches, bar[1] is a generation

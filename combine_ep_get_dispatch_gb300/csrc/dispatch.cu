@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
 // step's 2048 channels are quantised they leave by one bulk store
 // (cp.async.bulk shared->global) per destination row, while the next step is
 // quantised; the scales follow with plain stores (a UE8M0 scale row is not a
-// multiple of 16 bytes). Launched with at most 120 KB of staged rows per SM
-// (8 tokens of hidden 7168): every first-wave block loads its row at once, so
+// multiple of 16 bytes). Launched with at most 105 KB of staged rows per SM
+// (7 tokens of hidden 7168): every first-wave block loads its row at once, so
 // the cap shortens the read burst and the synchronous quantisation before the
 // first stores (measured on GB300: the 4096-token hidden-7168 dispatch went
 // from 85 to 79 us with the three changes; the PM-sampled DRAM timeline had
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
 // kernel's ramp and tail are too: four warps took the 4096-token FP8
 // dispatches from 90.1 to 86.0 us and 79.9 to 74.2 us).
 constexpr int kF8Warps = 4;                  // warps per token (one token per block)
-constexpr size_t kF8StagedBytesPerSM = 120 * 1024;  // see launch_fp8
+constexpr size_t kF8StagedBytesPerSM = 105 * 1024;  // see launch_fp8
 constexpr size_t kSmemPerSM = 228 * 1024;            // shared memory of one SM
 constexpr size_t kSmemReservedPerBlock = 1024;       // the runtime's share of it per block
 constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank copies
@@ -172,6 +172,27 @@ __device__ __forceinline__ float pow2_ceil(float s) {
 // UE8M0 byte 2^(b - 127) of a power-of-two scale >= 2^-127 (0 for s = 0).
 __device__ __forceinline__ uint8_t ue8m0_byte(float s) {
   return static_cast<uint8_t>((__float_as_uint(s) >> 23) & 0xFFu);
+}
+
+// Packed fp32 pairs (lo in the low word): the sm_100-family f32x2
+// arithmetic, one instruction for two IEEE fp32 operations.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
@@ -204,19 +225,27 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
       // remainder x - s * q0 is exact by a fused multiply-add, and
       // q0 + remainder * y rounds to x / s (Markstein's correction step,
       // "Computation of elementary functions on the IBM RISC System/6000
-      // processor", IBM J. Res. Dev. 34(1), 1990). A zero remainder keeps q0
-      // itself, so -0 / s stays -0. The remainder is exact only if it does
-      // not underflow: for |x / s| >= 2^-11 (below that every E4M3 code is
-      // a zero) it is a multiple of 2^(e_s - 57), which s >= 2^-92 keeps at
-      // or above 2^-149; s <= 2^126 keeps y normal. Smaller or larger scales
-      // take the IEEE division. A device test compares every (x, amax) pair
-      // of BF16 inputs with the oracle's IEEE division.
+      // processor", IBM J. Res. Dev. 34(1), 1990). The remainder is exact
+      // only if it does not underflow: for |x / s| >= 2^-11 (below that
+      // every E4M3 code is a zero) it is a multiple of 2^(e_s - 57), which
+      // s >= 2^-92 keeps at or above 2^-149; s <= 2^126 keeps y normal.
+      // Smaller or larger scales take the IEEE division. Two channels per
+      // instruction (packed fp32 pairs, each lane rounded as its own fp32
+      // operation). The quotient takes x's sign: the correction turns
+      // -0 / s into +0, every other quotient already has it. A device test
+      // compares every (x, amax) pair of BF16 inputs with the oracle's IEEE
+      // division.
       const float y = __frcp_rn(sc);
+      const uint64_t y2 = pack_f32x2(y, y), ns2 = pack_f32x2(-sc, -sc);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float q0 = f[i] * y;
-        const float r = fmaf(-sc, q0, f[i]);
-        f[i] = r == 0.0f ? q0 : fmaf(r, y, q0);
+      for (int i = 0; i < 16; i += 2) {
+        const uint64_t x2 = pack_f32x2(f[i], f[i + 1]);
+        const uint64_t q0 = mul_f32x2(x2, y2);
+        const uint64_t r = fma_f32x2(ns2, q0, x2);
+        float lo, hi;
+        unpack_f32x2(fma_f32x2(r, y2, q0), lo, hi);
+        f[i] = copysignf(lo, f[i]);
+        f[i + 1] = copysignf(hi, f[i + 1]);
       }
     } else {
 #pragma unroll
@@ -348,11 +377,12 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
     __syncthreads();
     return;
   }
-  // Step c0 covers channels [c0, c0 + 512 * kF8Warps), 512 per warp. Its codes
-  // go to bytes [c0, c0 + 512 * kF8Warps) of the row, which later steps never
-  // read; the barrier keeps them from overwriting this step's own inputs.
+  // Step c0 covers channels [c0, c0 + kStep), 512 per warp. Its codes go to
+  // bytes [c0, c0 + kStep) of the row, which later steps never read; the
+  // barrier keeps them from overwriting this step's own inputs.
+  constexpr int kStep = 512 * kF8Warps;
   int seg_lo = 0;
-  for (int c0 = 0; c0 < H; c0 += 512 * kF8Warps) {
+  for (int c0 = 0; c0 < H; c0 += kStep) {
     const int c = c0 + w * 512 + lane * 16;
     uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
     if (c < H) {
@@ -366,7 +396,7 @@ __global__ void __launch_bounds__(kF8Warps * 32) dispatch_fp8_kernel(const Dispa
       *reinterpret_cast<uint4*>(row + c) = q;
       if ((lane & 7) == 0) scales[c >> 7] = sc;
     }
-    const int hi = c0 + 512 * kF8Warps;
+    const int hi = c0 + kStep;
     if (!kLateDest && hi < H) {
       fence_proxy_async_smem();
       __syncthreads();
@@ -744,6 +774,10 @@ __device__ void ll_row(const LLSendParams& p, int t, int sp, uint8_t* smem) {
 template <bool kFp8, int KMAX>
 __global__ void __launch_bounds__(kLLRowThreads) ll_send_small_kernel(const LLSendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream (which may have produced x or the routing): wait for it first.
+  grid_dependency_wait();
+  launch_dependents();
   if (blockIdx.x == 0) {
     ll_table(p, reinterpret_cast<int32_t*>(smem));
     return;
@@ -756,6 +790,7 @@ __global__ void __launch_bounds__(kLLRowThreads) ll_send_small_kernel(const LLSe
 // its dependent row kernel at once.
 __global__ void __launch_bounds__(kLLHistThreads) ll_hist_kernel(const LLSendParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  grid_dependency_wait();  // launched as a programmatic dependent, like the small form
   launch_dependents();
   ll_source_hist(p, reinterpret_cast<int32_t*>(smem));
 }
@@ -805,7 +840,7 @@ cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s, bool pdl) {
   size_t smem = kBarBytes + f8_warp_bytes(p.H);
   const size_t blocks = kF8StagedBytesPerSM / smem;
   if (blocks >= 1 && blocks < kSmemPerSM / (smem + kSmemReservedPerBlock)) {
-    const size_t capped = kSmemPerSM / blocks - kSmemReservedPerBlock;
+    const size_t capped = kSmemPerSM / blocks - kSmemReservedPerBlock - 256;
     if (capped > smem) smem = capped;
   }
   void (*fn)(DispatchParams) = pdl ? dispatch_fp8_kernel<true> : dispatch_fp8_kernel<false>;
@@ -840,8 +875,7 @@ cudaError_t launch_ll_rows_variant(const LLSendParams& p, unsigned grid, size_t 
     void (*fn)(LLSendParams) = ll_send_small_kernel<kFp8, KMAX>;
     const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
     if (err != cudaSuccess) return err;
-    fn<<<grid, kLLRowThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3(grid), dim3(kLLRowThreads), smem, s, /*dependent=*/true, p);
   }
   void (*fn)(LLSendParams) = ll_send_rows_kernel<kFp8, KMAX>;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), current_device(), smem);
@@ -887,8 +921,8 @@ cudaError_t launch_ll_send(LLSendParams p, cudaStream_t s) {
   const size_t table_smem = sizeof(int32_t) * (static_cast<size_t>(p.E) * (p.R + 1) + p.E);
   if (mid) {
     if (!p.hist) return cudaErrorInvalidValue;
-    ll_hist_kernel<<<p.R, kLLHistThreads, sizeof(int32_t) * p.E, s>>>(p);
-    const cudaError_t lerr = cudaGetLastError();
+    const cudaError_t lerr = launch_kernel(ll_hist_kernel, dim3(p.R), dim3(kLLHistThreads), sizeof(int32_t) * p.E,
+                                           s, /*dependent=*/true, p);
     if (lerr != cudaSuccess) return lerr;
   }
   // Block 0 of the larger form's row kernel needs no shared table.

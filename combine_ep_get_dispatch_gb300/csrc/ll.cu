@@ -29,6 +29,11 @@ constexpr int kRecvUnroll = 8;  // ranges per thread with their loads in flight 
 __global__ void __launch_bounds__(kRecvThreads) ll_recv_kernel(const LLRecvParams p, int E, int R) {
   __shared__ int s_ok;
   const int tid = threadIdx.x;
+  // Launched as a programmatic dependent (the send before it drains while
+  // this block is scheduled): wait for it before reading the workspace, and
+  // let the next kernel on the stream be scheduled at once.
+  grid_dependency_wait();
+  launch_dependents();
   LLHeader h{};
   if (tid == 0) h = *p.hdr;  // written by an earlier launch on this stream
   const int32_t c = tid < E ? p.count[tid] : 0;
@@ -96,8 +101,7 @@ __global__ void e4m3_encode_kernel(const float* __restrict__ in, uint8_t* __rest
 }  // namespace
 
 cudaError_t launch_ll_recv(const LLRecvParams& p, int E, int R, cudaStream_t s) {
-  ll_recv_kernel<<<1, kRecvThreads, 0, s>>>(p, E, R);
-  return cudaGetLastError();
+  return launch_kernel(ll_recv_kernel, dim3(1), dim3(kRecvThreads), 0, s, /*dependent=*/true, p, E, R);
 }
 
 cudaError_t launch_ll_mask(int32_t* mask, int R, int mode, int rank, int value, int32_t* out, cudaStream_t s) {

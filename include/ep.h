@@ -34,6 +34,14 @@
  *     bits into it for data-dependent conditions (an expert index out of
  *     range, a destination row beyond a buffer's capacity, ...). The
  *     offending row is skipped; no kernel traps. The caller zeroes it.
+ *   - The combines, the low-latency send (up to 65536 entries) and the
+ *     receive launch their first kernel as a programmatic dependent of the
+ *     kernel before it on the stream: it may be scheduled while that kernel
+ *     drains, and it waits for that kernel to complete before it reads or
+ *     writes any memory, so stream order holds as for a plain launch. (If
+ *     the kernel before it was itself launched by the caller with
+ *     programmatic serialization and never waits for its own predecessor,
+ *     that predecessor is not waited for either.)
  *   - BF16 data is passed as raw 16-bit words, E4M3 data as bytes.
  *   - Row buffers (x, receive buffers, expert outputs, out) must be 16-byte
  *     aligned, and hidden * element size must be a multiple of 16 bytes.
