@@ -391,15 +391,17 @@ size_t ep_ll_workspace_bytes(int num_tokens, int num_topk, int num_experts, int 
  *   status       EP_ST_BAD_INDEX, EP_ST_TIMEOUT and EP_ST_WORKSPACE as for
  *                the layout
  * Slots of ranks masked in the workspace (shrink mode, ep_ll_update_mask)
- * are dropped. A small batch (N * K <= 4096 and E * R <= 16384) is one
- * launch: every block finds the slots of its own token from the whole
- * routing table, one block writes the counts and ranges. A larger batch is
- * two launches: the routing layout, then the row copies as its programmatic
- * dependent (they load and quantise their rows while the layout runs, and
- * wait for it in-kernel before reading a slot); the second may fail with
- * EP_ERR_CUDA after the first was enqueued. The rows are in place when the
- * stream reaches the end of this call; the counts are published by
- * ep_ll_dispatch_recv.
+ * are dropped. With E * R <= 16384, a batch of N * K <= 4096 entries is one
+ * launch (every block finds its own token's slots from the whole routing
+ * table; one block writes the counts and ranges), and a batch of up to 65536
+ * entries with (N / R) * K <= 8192 is two: per-source-rank histograms, then
+ * the row copies as their programmatic dependent (they load, count their own
+ * source rank's earlier entries and quantise while the histograms are built,
+ * then add the earlier source ranks' counts). Otherwise it is two launches:
+ * the routing layout, then the row copies as its programmatic dependent. A
+ * second launch may fail with EP_ERR_CUDA after the first was enqueued. The
+ * rows are in place when the stream reaches the end of this call; the counts
+ * are published by ep_ll_dispatch_recv.
  */
 int ep_ll_dispatch_send(const void* x, const int32_t* topk_idx, int num_tokens, int num_topk,
                         int hidden, int num_experts, int num_ranks, int max_tokens_per_rank,
