@@ -116,6 +116,15 @@ def test_host_validation_rejects_before_cuda(L):
     assert L.ep_ll_combine(P(16), P(16), None, P(256), 1 << 30, 128, 8, 100, 256, 8, 128, P(16), None, None) \
         == ep.EP_ERR_INVALID_ARG  # hidden % 8 != 0
     assert L.ep_fp8_e4m3_encode(None, None, -1, None) == ep.EP_ERR_INVALID_ARG
+    # quantisation on its own: FP8 flag required, hidden % 128, 16-byte rows, buffers for rows > 0
+    Q = L.ep_fp8_quantize
+    assert Q(P(16), 4, 256, 0, P(16), P(16), None) == ep.EP_ERR_INVALID_ARG          # BF16 flag word
+    assert Q(P(16), 4, 200, ep.EP_FP8, P(16), P(16), None) == ep.EP_ERR_INVALID_ARG  # hidden % 128 != 0
+    assert Q(P(16), -1, 256, ep.EP_FP8, P(16), P(16), None) == ep.EP_ERR_INVALID_ARG
+    assert Q(P(16), 4, 256, ep.EP_FP8, P(16), None, None) == ep.EP_ERR_INVALID_ARG   # no scale buffer
+    assert Q(P(24), 4, 256, ep.EP_FP8, P(16), P(16), None) == ep.EP_ERR_ALIGNMENT
+    assert Q(P(16), 4, 256, ep.EP_FP8, P(40), P(16), None) == ep.EP_ERR_ALIGNMENT
+    assert Q(None, 0, 256, ep.EP_FP8 | ep.EP_FP8_UE8M0, None, None, None) == ep.EP_OK  # nothing to do
     # shrink-mode mask calls: rank range, rank count, workspace size
     assert L.ep_ll_update_mask(P(256), 1 << 20, 8, 8, 1, None) == ep.EP_ERR_INVALID_ARG
     assert L.ep_ll_update_mask(P(256), 1 << 20, 0, 0, 1, None) == ep.EP_ERR_INVALID_ARG

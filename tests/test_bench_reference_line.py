@@ -27,3 +27,29 @@ def test_reference_line_keys():
     c = d["config"]
     assert c["workload"].startswith("ll_decode_tiny") and c["tokens"] == 128 and c["topk"] == 8
     assert c["rows"] == {"received": 1024}   # 128 tokens x 8 routed slots, none masked
+
+
+def test_default_run_measures_every_workload():
+    """bench.py's default run (the large prefill, no variant flag) also measures
+    workloads 1, 2, 3 and 5; a chosen workload, a token override or a variant
+    flag measures that configuration alone."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def extras(*argv):
+        old = sys.argv
+        sys.argv = ["bench.py", *argv]
+        try:
+            return bench.extra_workloads(bench.parse())
+        finally:
+            sys.argv = old
+
+    assert extras() == [1, 2, 3, 5]
+    assert extras("--steps", "20", "--warmup", "5") == [1, 2, 3, 5]
+    assert extras("--workload", "3") == []
+    assert extras("--tokens", "4096") == []
+    assert extras("--graph") == []
+    assert extras("--fp8-scales", "ue8m0") == []
+    assert extras("--extra-workloads", "none") == []
+    assert extras("--workload", "1", "--extra-workloads", "2,3") == [2, 3]
