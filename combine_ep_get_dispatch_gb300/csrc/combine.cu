@@ -25,6 +25,12 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kChunk = 8;
 
+// Barrier `id` (1..15; 0 is __syncthreads) over the first `threads` threads
+// of the block (a multiple of 32, whole warps).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void fma8(float* acc, float w, const uint4& v) {
   acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
   acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
@@ -47,13 +53,13 @@ __device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b)
 // low-latency combine).
 template <bool kGather>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int nchunk) {
-  extern __shared__ int32_t s_dyn[];  // the token's routed slots, in order: rows, weights, slot index
+  // The token's routed slots in order: expert row, weight, slot index; and
+  // the weights by slot.
+  __shared__ int32_t s_row[EP_MAX_TOPK], s_k[EP_MAX_TOPK];
+  __shared__ float s_w[EP_MAX_TOPK], s_wk[EP_MAX_TOPK];
   __shared__ int s_ok, s_nv;
   const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K, H = p.H;
-  int32_t* s_row = s_dyn;
-  float* s_w = reinterpret_cast<float*>(s_dyn + K);
-  int32_t* s_k = s_dyn + 2 * K;
   // Launched as a programmatic dependent: nothing is touched before the
   // kernel ahead of it on the stream has completed.
   grid_dependency_wait();
@@ -81,33 +87,37 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     const int v1 = min(nvec, v0 + span);
     // Warp 0 lists the routed slots in slot order (masked ones dropped), so
     // every row load below is useful and all of them go out in one round
-    // whenever a token has at most kChunk routed slots.
+    // whenever a token has at most kChunk routed slots. K <= 32: a lane per
+    // slot. Warp 1 fetches the weights meanwhile (by slot), and warp 0 copies
+    // them into list order once both warps are past the named barrier.
     if (tid < 32) {
-      int nv = 0;
-      for (int k0 = 0; k0 < K; k0 += 32) {
-        const int k = k0 + lane;
-        int32_t row = k < K ? __ldg(p.slot + t * K + k) : -1;
-        // Low-latency shrink mode: skip the slots of ranks masked now (the
-        // expert's rank, from its region e = row / (R*T), or the token's source).
-        if (row >= 0 && p.rank_mask &&
-            (__ldg(p.rank_mask + static_cast<int>(row / p.ll_cap) / p.ll_L) != 0 ||
-             __ldg(p.rank_mask + static_cast<int>(t / p.ll_ns)) != 0))
-          row = -1;
-        if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + k);
-        if (row >= p.y_rows) {
-          flag(p.status, EP_ST_CAPACITY);
-          row = -1;
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, row >= 0);
-        if (row >= 0) {
-          const int pos = nv + __popc(m & lanemask_lt());
-          s_row[pos] = row;
-          s_w[pos] = p.w ? __ldg(p.w + t * K + k) : 1.0f;
-          s_k[pos] = k;
-        }
-        nv += __popc(m);
+      const int k = lane;
+      int32_t row = k < K ? __ldg(p.slot + t * K + k) : -1;
+      // Low-latency shrink mode: skip the slots of ranks masked now (the
+      // expert's rank, from its region e = row / (R*T), or the token's source).
+      if (row >= 0 && p.rank_mask &&
+          (__ldg(p.rank_mask + static_cast<int>(row / p.ll_cap) / p.ll_L) != 0 ||
+           __ldg(p.rank_mask + static_cast<int>(t / p.ll_ns)) != 0))
+        row = -1;
+      if (row >= 0 && p.token_major) row = static_cast<int32_t>(t * K + k);
+      if (row >= p.y_rows) {
+        flag(p.status, EP_ST_CAPACITY);
+        row = -1;
       }
-      if (lane == 0) s_nv = nv;
+      const unsigned m = __ballot_sync(0xffffffffu, row >= 0);
+      const int pos = __popc(m & lanemask_lt());
+      if (row >= 0) {
+        s_row[pos] = row;
+        s_k[pos] = k;
+      }
+      if (lane == 0) s_nv = __popc(m);
+      if (!kGather) {
+        named_barrier_sync(1, 64);
+        if (row >= 0) s_w[pos] = s_wk[k];
+      }
+    } else if (!kGather && tid < 64) {
+      if (lane < K) s_wk[lane] = p.w ? __ldg(p.w + t * K + lane) : 1.0f;
+      named_barrier_sync(1, 64);
     }
     __syncthreads();
     const int nv = s_nv;
@@ -170,8 +180,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(p.N) * nchunk;
   const int64_t cap = int64_t(1) << 30;
   const int grid = static_cast<int>(items < cap ? items : cap);
-  const size_t smem = static_cast<size_t>(p.K) * 12;
-  return launch_kernel(p.gather ? combine_kernel<true> : combine_kernel<false>, dim3(grid), dim3(kThreads), smem, s,
+  return launch_kernel(p.gather ? combine_kernel<true> : combine_kernel<false>, dim3(grid), dim3(kThreads), 0, s,
                        /*dependent=*/true, p, nchunk);
 }
 
@@ -192,6 +201,7 @@ __global__ void __launch_bounds__(kThreads) combine_to_ranks_kernel(const Combin
     if (tid < K) {
       const int e = __ldg(p.idx + t * K + tid);
       int32_t row = __ldg(p.expert_slot + t * K + tid);
+      const float wk = __ldg(p.w + t * K + tid);
       const bool ok = e >= 0 && e < E && row >= 0;
       if (ok && row >= p.y_rows) {
         flag(p.status, EP_ST_CAPACITY);
@@ -200,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) combine_to_ranks_kernel(const Combin
       const int r = (ok && row >= 0) ? e / L : -1;
       s_rank[tid] = r;
       s_row[tid] = row;
-      s_w[tid] = __ldg(p.w + t * K + tid);
+      s_w[tid] = wk;
       int32_t orow = -1;
       if (r >= 0) {
         orow = __ldg(p.rank_slot + t * R + r);
@@ -297,12 +307,13 @@ __global__ void __launch_bounds__(kThreads) combine_backward_kernel(const Combin
   for (int64_t t = blockIdx.x; t < p.N; t += gridDim.x) {
     if (tid < K) {
       int32_t row = __ldg(p.slot + t * K + tid);
+      const float wk = __ldg(p.w + t * K + tid);
       if (row >= p.y_rows) {
         flag(p.status, EP_ST_CAPACITY);
         row = -1;
       }
       s_row[tid] = row;
-      s_w[tid] = __ldg(p.w + t * K + tid);
+      s_w[tid] = wk;
     }
     __syncthreads();
     const uint4* g_row = reinterpret_cast<const uint4*>(p.grad_out + t * H);

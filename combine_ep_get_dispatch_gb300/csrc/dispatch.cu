@@ -67,23 +67,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
   // this kernel may have started before the layout finished (the row load
   // above needs nothing from it).
   grid_dependency_wait();
-  // This lane's top-k slot (lane < K): expert, weight and expert-major row.
+  // This lane's top-k slot (lane < K): expert, weight and expert-major row;
+  // and its first rank's per-rank row. Every lookup goes out before any
+  // store (a store through a pointer that may alias would hold back the
+  // loads after it).
   int e_k = -1;
   float w_k = 0.0f;
   int32_t erow = -1;
   if (lane < K) {
     e_k = __ldg(p.idx + t * K + lane);
     if (p.w) w_k = __ldg(p.w + t * K + lane);
-    if (p.exp_x) {
-      erow = __ldcg(p.expert_slot + t * K + lane);
-      if (erow >= p.exp_cap) {
-        flag(p.status, p.overflow_bit);
-        erow = -1;
-      }
-      if (erow >= 0 && p.exp_src)
-        p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
-    }
+    if (p.exp_x) erow = __ldcg(p.expert_slot + t * K + lane);
   }
+  int32_t rrow0 = (p.rank_x && lane < R) ? __ldcg(p.rank_slot + t * R + lane) : -1;
+  const int rank_k = (e_k >= 0 && e_k < E) ? e_k / L : -1;
+  const int local_k = e_k - rank_k * L;
+  if (erow >= p.exp_cap) {
+    flag(p.status, p.overflow_bit);
+    erow = -1;
+  }
+  if (erow >= 0 && p.exp_src)
+    p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
 
   // Every lane sees the row land itself (its stores read it); the warp
   // leaves together if any lane's bounded wait gave up.
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
   if (p.rank_x) {
     for (int r0 = 0; r0 < R; r0 += 32) {
       const int r = r0 + lane;
-      int32_t rrow = (r < R) ? __ldcg(p.rank_slot + t * R + r) : -1;
+      int32_t rrow = r0 == 0 ? rrow0 : ((r < R) ? __ldcg(p.rank_slot + t * R + r) : -1);
       if (rrow >= p.rank_cap) {
         flag(p.status, EP_ST_CAPACITY);
         rrow = -1;
@@ -115,11 +119,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
       }
       if (p.rank_topk_idx || p.rank_topk_w) {
         for (int kk = 0; kk < K; ++kk) {
-          const int ek = __shfl_sync(0xffffffffu, e_k, kk);
+          const int rk = __shfl_sync(0xffffffffu, rank_k, kk);
+          const int lk = __shfl_sync(0xffffffffu, local_k, kk);
           const float wk = __shfl_sync(0xffffffffu, w_k, kk);
           if (rrow >= 0) {
-            const bool here = ek >= 0 && ek < E && ek / L == r;
-            if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? ek - r * L : -1;
+            const bool here = rk == r;
+            if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? lk : -1;
             if (p.rank_topk_w) p.rank_topk_w[static_cast<int64_t>(rrow) * K + kk] = here ? wk : 0.0f;
           }
         }
@@ -277,16 +282,20 @@ __host__ __device__ inline unsigned f8_warp_bytes(int H) {
 __device__ __forceinline__ int f8_destinations(const DispatchParams& p, int64_t t, int lane, int e_k, float w_k,
                                                int32_t* drow, int& ne) {
   const int K = p.K, R = p.R, L = p.L, E = p.E;
-  int32_t erow = -1;
-  if (lane < K && p.exp_x) {
-    erow = __ldcg(p.expert_slot + t * K + lane);
-    if (erow >= p.exp_cap) {
-      flag(p.status, p.overflow_bit);
-      erow = -1;
-    }
-    if (erow >= 0 && p.exp_src)
-      p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
+  // Every lookup goes out before any store below: the stores go through
+  // pointers the compiler must assume may alias the slot arrays, so a load
+  // issued after one waits for it.
+  int32_t erow = (lane < K && p.exp_x) ? __ldcg(p.expert_slot + t * K + lane) : -1;
+  int32_t rrow = (p.rank_x && lane < R) ? __ldcg(p.rank_slot + t * R + lane) : -1;
+  // This slot's rank and local expert id, for the per-rank top-k metadata.
+  const int rank_k = (e_k >= 0 && e_k < E) ? e_k / L : -1;
+  const int local_k = e_k - rank_k * L;
+  if (erow >= p.exp_cap) {
+    flag(p.status, p.overflow_bit);
+    erow = -1;
   }
+  if (erow >= 0 && p.exp_src)
+    p.exp_src[erow] = p.exp_src_is_token ? static_cast<int32_t>(t) : static_cast<int32_t>(t * K + lane);
   const unsigned vm = __ballot_sync(0xffffffffu, erow >= 0);
   if (erow >= 0) drow[__popc(vm & lanemask_lt())] = erow;
   ne = __popc(vm);
@@ -294,7 +303,7 @@ __device__ __forceinline__ int f8_destinations(const DispatchParams& p, int64_t 
   if (p.rank_x) {
     for (int rb = 0; rb < R; rb += 32) {
       const int r = rb + lane;
-      int32_t rrow = (r < R) ? __ldcg(p.rank_slot + t * R + r) : -1;
+      if (rb > 0) rrow = (r < R) ? __ldcg(p.rank_slot + t * R + r) : -1;
       if (rrow >= p.rank_cap) {
         flag(p.status, EP_ST_CAPACITY);
         rrow = -1;
@@ -309,11 +318,12 @@ __device__ __forceinline__ int f8_destinations(const DispatchParams& p, int64_t 
       n = min(n + __popc(rm), kF8MaxDest);
       if (p.rank_topk_idx || p.rank_topk_w) {
         for (int kk = 0; kk < K; ++kk) {
-          const int ek = __shfl_sync(0xffffffffu, e_k, kk);
+          const int rk = __shfl_sync(0xffffffffu, rank_k, kk);
+          const int lk = __shfl_sync(0xffffffffu, local_k, kk);
           const float wk = __shfl_sync(0xffffffffu, w_k, kk);
           if (rrow >= 0) {
-            const bool here = ek >= 0 && ek < E && ek / L == r;
-            if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? ek - r * L : -1;
+            const bool here = rk == r;
+            if (p.rank_topk_idx) p.rank_topk_idx[static_cast<int64_t>(rrow) * K + kk] = here ? lk : -1;
             if (p.rank_topk_w) p.rank_topk_w[static_cast<int64_t>(rrow) * K + kk] = here ? wk : 0.0f;
           }
         }
