@@ -83,7 +83,9 @@ def parse():
                     help="normal workloads: layout and dispatch through one call (ep_layout_dispatch), timed as one phase")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=None,
+                    help="tokens of the workload the oracle baseline runs on (default: all of them); its time "
+                         "is bounded by repetitions, about 10 s on every core and 5 s on one")
     ap.add_argument("--l2-flush", default="write", choices=["write", "write-read"],
                     help="between steps: write 256 MiB (default), or write it and read it back so that no "
                          "dirty line of the flush is left in L2 when the step starts")
@@ -224,6 +226,7 @@ class NormalWorkload:
         self.align, self.two_level = max(1, align), two_level
         sdt = torch.uint8 if scales == "ue8m0" else torch.float32
         N, H, K, E, R = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R
+        self.inp = inp   # the host inputs (the oracle baseline reuses them)
         self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
         self.idx_host = torch.from_numpy(inp["topk_idx"])
         self.w_host = torch.from_numpy(inp["topk_weights"])
@@ -370,6 +373,7 @@ class LLWorkload:
         self.flags = fp8_flag_word(ep, cfg, scales)
         self.scale_bytes = 1 if scales == "ue8m0" else 4
         N, H, K, E, R, T = cfg.N, cfg.H, cfg.K, cfg.E, cfg.R, cfg.T
+        self.inp = inp   # the host inputs (the oracle baseline reuses them)
         self.x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16)
         self.idx_host = torch.from_numpy(inp["topk_idx"])
         self.w_host = torch.from_numpy(inp["topk_weights"])
@@ -764,7 +768,7 @@ def run_ours(args):
                                 "ms_per_step": round(extra_e2e[w], 4)}
             line["workloads"][c2.name] = entry
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_sample_tokens)
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_sample_tokens, wl.inp)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -784,19 +788,23 @@ def _oracle_step(sub):
     oracle.combine(y, lay["expert_slot"], sub["topk_weights"])
 
 
-def _sample(cfg, n_tok):
+def _sample(cfg, n_tok, inp=None):
+    """The first n_tok tokens' inputs (all of them for None); `inp`, the whole
+    workload's inputs when already made, is reused for the whole workload."""
+    if n_tok is None:
+        n_tok = cfg.N
     if cfg.mode == "ll":
         n_tok = max(cfg.R, (min(n_tok, cfg.N) // cfg.R) * cfg.R)
     else:
         n_tok = min(n_tok, cfg.N)
-    d = ei.make_inputs(cfg.scaled(N=n_tok), seed=0)
+    d = dict(inp) if (inp is not None and n_tok == cfg.N) else ei.make_inputs(cfg.scaled(N=n_tok), seed=0)
     # Low latency: the sample's own per-rank capacity (rows do not depend on T).
     T = max(1, n_tok // cfg.R) if cfg.mode == "ll" else None
     d.update(E=cfg.E, R=cfg.R, T=T, fp8=cfg.fp8, mode=cfg.mode, n_tok=n_tok)
     return d
 
 
-def _time_oracle(sub, budget_s=10.0, max_reps=20):
+def _time_oracle(sub, budget_s, max_reps=1000):
     _oracle_step(sub)  # warm the library and the page cache
     reps, t = 0, 0.0
     while t < budget_s and reps < max_reps:
@@ -807,16 +815,16 @@ def _time_oracle(sub, budget_s=10.0, max_reps=20):
     return reps, t
 
 
-def cpu_baseline(cfg, n_tok):
+def cpu_baseline(cfg, n_tok, inp=None):
     """The oracle on the first n_tok tokens of the workload (the whole step on
     those tokens), on every host core (its OpenMP build: the row loops of
     dispatch and combine in parallel, the layout sequential, identical
     results), with the plain single-threaded build's figure beside it."""
     import oracle
-    sub = _sample(cfg, n_tok)
+    sub = _sample(cfg, n_tok, inp)
     n_tok = sub["n_tok"]
     oracle.use_all_cores(False)
-    reps1, t1 = _time_oracle(sub)
+    reps1, t1 = _time_oracle(sub, budget_s=5.0)
     one = {"value": round(n_tok * reps1 / t1, 1), "unit": "tokens/s", "cores": 1,
            "sample": f"{n_tok} of {cfg.N} tokens, {reps1} reps, {t1:.1f} s"}
     if not oracle.use_all_cores(True):
@@ -824,7 +832,7 @@ def cpu_baseline(cfg, n_tok):
                                                      f"those tokens), {reps1} reps, {t1:.1f} s; no OpenMP build"}
     try:
         cores = oracle.threads()
-        reps, t = _time_oracle(sub)
+        reps, t = _time_oracle(sub, budget_s=10.0)
     finally:
         oracle.use_all_cores(False)
     return {"value": round(n_tok * reps / t, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",

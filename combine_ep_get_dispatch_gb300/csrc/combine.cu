@@ -46,13 +46,14 @@ __device__ __forceinline__ bool same_shape(const LLHeader& a, const LLHeader& b)
   return a.N == b.N && a.K == b.K && a.E == b.E && a.R == b.R && a.T == b.T;
 }
 
-// Block b handles token b / nchunk and the b % nchunk-th of nchunk equal
-// spans of its row (nchunk > 1 only when there are few tokens: it spreads a
-// small batch over more SMs). kGather copies each routed row to its own
-// output row t*K + k instead of summing (the send half of the two-phase
-// low-latency combine).
+// The first N - tail tokens are one work item each (the whole row); each of
+// the last `tail` tokens is nchunk items, equal spans of its row. Splitting
+// the tail shortens the blocks that run while the grid drains; a small batch
+// is all tail (it spreads over more SMs). Blocks take items in order.
+// kGather copies each routed row to its own output row t*K + k instead of
+// summing (the send half of the two-phase low-latency combine).
 template <bool kGather>
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int nchunk) {
+__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p, int64_t tail, int nchunk) {
   // The token's routed slots in order: expert row, weight, slot index; and
   // the weights by slot.
   __shared__ int32_t s_row[EP_MAX_TOPK], s_k[EP_MAX_TOPK];
@@ -80,11 +81,17 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
   }
   const int nvec = H / 8;
   const int span = (nvec + nchunk - 1) / nchunk;
-  const int64_t items = static_cast<int64_t>(p.N) * nchunk;
+  const int64_t head = p.N - tail;
+  const int64_t items = head + tail * nchunk;
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-    const int64_t t = it / nchunk;
-    const int v0 = static_cast<int>(it - t * nchunk) * span;
-    const int v1 = min(nvec, v0 + span);
+    int64_t t = it;
+    int v0 = 0, v1 = nvec;
+    if (it >= head) {
+      const int64_t j = it - head;
+      t = head + j / nchunk;
+      v0 = static_cast<int>(j - (t - head) * nchunk) * span;
+      v1 = min(nvec, v0 + span);
+    }
     // Warp 0 lists the routed slots in slot order (masked ones dropped), so
     // every row load below is useful and all of them go out in one round
     // whenever a token has at most kChunk routed slots. K <= 32: a lane per
@@ -165,23 +172,32 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
   if (p.N <= 0) return cudaSuccess;
   // One block per token (the hardware scheduler hands blocks to SMs as they
-  // free up); a batch with fewer tokens than eight blocks per SM splits each
-  // row into up to nvec / 128 spans.
+  // free up), at most eight resident per SM (64 registers). The tokens past
+  // the last multiple of eight per SM (the last partial wave) are split into
+  // as many spans as a row has 128-vector groups, so the blocks still running
+  // while the grid drains are short; measured against whole-token blocks:
+  // -1.6 us on 16384 tokens at hidden 7168, -2.7 us on 4096. A batch with
+  // fewer tokens than that splits every row, up to the same limit.
   const int sms = device_sms(current_device());
   const int nvec = p.H / 8;
-  int nchunk = 1;
+  const int most = (nvec + kThreads - 1) / kThreads;
   const int64_t want = static_cast<int64_t>(sms) * 8;
+  int nchunk = most;
+  int64_t tail = p.N % want;
   if (p.N < want) {
     nchunk = static_cast<int>((want + p.N - 1) / p.N);
-    const int most = (nvec + kThreads - 1) / kThreads;
     if (nchunk > most) nchunk = most;
-    if (nchunk < 1) nchunk = 1;
+    tail = p.N;
   }
-  const int64_t items = static_cast<int64_t>(p.N) * nchunk;
+  if (nchunk <= 1) {
+    nchunk = 1;
+    tail = 0;
+  }
+  const int64_t items = (p.N - tail) + tail * nchunk;
   const int64_t cap = int64_t(1) << 30;
   const int grid = static_cast<int>(items < cap ? items : cap);
   return launch_kernel(p.gather ? combine_kernel<true> : combine_kernel<false>, dim3(grid), dim3(kThreads), 0, s,
-                       /*dependent=*/true, p, nchunk);
+                       /*dependent=*/true, p, tail, nchunk);
 }
 
 // ---- two-level combine, first level --------------------------------------------

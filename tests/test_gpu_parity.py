@@ -346,8 +346,11 @@ def _expert_outputs(n_rows, H, seed):
     return ei.bf16_bits_from_f32(z).reshape(n_rows, H)
 
 
+# Batches of at least eight blocks per SM (1216 tokens on 152 SMs) split the
+# last partial wave's tokens into spans: 1500 and 2500 tokens (ragged spans at
+# H 7296), 1217 (a one-token tail of two spans at H 1032), 2432 (no tail).
 @pytest.mark.parametrize("c,N,H", [(3, 1000, 7168), (4, 777, 7168), (5, 1500, 4096), (4, 129, 8),
-                                   (5, 100, 1032)])
+                                   (5, 100, 1032), (4, 2500, 7296), (3, 1217, 1032), (3, 2432, 7168)])
 def test_combine_parity(c, N, H):
     cfg = ei.WORKLOADS[c].scaled(N=N, H=H)
     idx, w = ei.make_routing(cfg, seed=c + 10)
