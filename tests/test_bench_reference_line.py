@@ -53,3 +53,30 @@ def test_default_run_measures_every_workload():
     assert extras("--fp8-scales", "ue8m0") == []
     assert extras("--extra-workloads", "none") == []
     assert extras("--workload", "1", "--extra-workloads", "2,3") == [2, 3]
+
+
+def test_cpu_baseline_runs_on_the_whole_workload_by_default():
+    """Without --cpu-sample-tokens the oracle baseline takes every token of the
+    workload, reusing the host inputs the GPU arm made; a smaller sample is
+    drawn afresh from the same seeded generator (its first tokens)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import epinputs as ei
+
+    old = sys.argv
+    sys.argv = ["bench.py"]
+    try:
+        assert bench.parse().cpu_sample_tokens is None
+    finally:
+        sys.argv = old
+    cfg = ei.WORKLOADS[3].scaled(N=64, H=256)
+    inp = ei.make_inputs(cfg, seed=0)
+    whole = bench._sample(cfg, None, inp)
+    assert whole["n_tok"] == 64 and whole["x"] is inp["x"] and whole["topk_idx"] is inp["topk_idx"]
+    part = bench._sample(cfg, 16, inp)
+    assert part["n_tok"] == 16 and part["x"] is not inp["x"]
+    assert np.array_equal(part["x"], inp["x"][:16])
+    ll = ei.WORKLOADS[1].scaled(N=64, H=256)
+    assert bench._sample(ll, 20, None)["n_tok"] == 16        # whole source ranks (8 ranks)
