@@ -439,6 +439,31 @@ def test_ll_dispatch_parity(c, n_s, H, T):
     assert status_value(st) == 0
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_empty_batches(fp8):
+    """Zero tokens through every call: layout, dispatch and combine of the
+    normal path; low-latency send, receive and combine (all counts and ranges
+    zero, no status bit)."""
+    H, K, E, R, T = 256, 4, 32, 4, 8
+    st = _status()
+    x0 = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    i0 = torch.empty((0, K), dtype=torch.int32, device="cuda")
+    w0 = torch.empty((0, K), dtype=torch.float32, device="cuda")
+    lay = ep.get_dispatch_layout(i0, E, R, status=st)
+    _layout_equal(lay, oracle.layout(np.zeros((0, K), np.int32), E, R))
+    ep.dispatch(x0, lay, w0, use_fp8=fp8, status=st)
+    out = ep.combine(torch.zeros((1, H), dtype=torch.bfloat16, device="cuda"), lay, w0, status=st)
+    assert tuple(out.shape) == (0, H)
+    recv, cnt, handle, hook = ep.low_latency_dispatch(x0, i0, T, E, R, use_fp8=fp8, status=st)
+    hook()
+    assert cnt.cpu().numpy().tolist() == [0] * E
+    assert not handle.layout_range.cpu().numpy().any()
+    outl = ep.low_latency_combine(torch.zeros((E, R * T, H), dtype=torch.bfloat16, device="cuda"), w0, handle,
+                                  status=st)
+    assert tuple(outl.shape) == (0, H)
+    assert status_value(st) == 0
+
+
 @pytest.mark.parametrize("E,R,n_s,K", [
     (4, 2, 2, 4),        # 16 entries: the one-launch send
     (1024, 32, 4, 8),    # E * R above the one-launch table: one-CTA layout + dispatch
