@@ -204,6 +204,20 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
 }
 
+// Per half of two packed BF16 pairs: max(|a|, |b|) (exact, as any max is),
+// with a sign bit the caller drops.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// The sign bits of four BF16 values (two packed pairs, in channel order)
+// placed at bit 7 of four code bytes.
+__device__ __forceinline__ uint32_t bf16_signs4(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x7531) & 0x80808080u;
+}
+
 // 16 BF16 channels of one lane -> 16 E4M3 codes; the 8 lanes of a 128-channel
 // block share the block's scale s = amax / 448, raised to a power of two with
 // EP_FP8_ROUND_SCALE, and also kept >= 2^-127 with EP_FP8_UE8M0 (all 32 lanes
@@ -214,9 +228,16 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
   f[4] = bf16_lo(v0.z); f[5] = bf16_hi(v0.z); f[6] = bf16_lo(v0.w); f[7] = bf16_hi(v0.w);
   f[8] = bf16_lo(v1.x); f[9] = bf16_hi(v1.x); f[10] = bf16_lo(v1.y); f[11] = bf16_hi(v1.y);
   f[12] = bf16_lo(v1.z); f[13] = bf16_hi(v1.z); f[14] = bf16_lo(v1.w); f[15] = bf16_hi(v1.w);
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+  uint32_t m2 = bf16x2_absmax(v0.x, v0.y);
+  m2 = bf16x2_absmax(m2, v0.z);
+  m2 = bf16x2_absmax(m2, v0.w);
+  m2 = bf16x2_absmax(m2, v1.x);
+  m2 = bf16x2_absmax(m2, v1.y);
+  m2 = bf16x2_absmax(m2, v1.z);
+  m2 = bf16x2_absmax(m2, v1.w);
+  // (fmaxf returns the other operand for a NaN: a NaN channel is left out of
+  // the amax, as when the maximum is taken over each channel in turn from 0.)
+  float m = fmaxf(0.0f, fmaxf(__uint_as_float((m2 << 16) & 0x7FFFFFFFu), __uint_as_float(m2 & 0x7FFF0000u)));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
   m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -236,10 +257,10 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
       // s >= 2^-92 keeps at or above 2^-149; s <= 2^126 keeps y normal.
       // Smaller or larger scales take the IEEE division. Two channels per
       // instruction (packed fp32 pairs, each lane rounded as its own fp32
-      // operation). The quotient takes x's sign: the correction turns
-      // -0 / s into +0, every other quotient already has it. A device test
-      // compares every (x, amax) pair of BF16 inputs with the oracle's IEEE
-      // division.
+      // operation). The codes take x's sign at the end: the correction
+      // turns -0 / s into +0, every other quotient already has it. A device
+      // test compares every (x, amax) pair of BF16 inputs with the oracle's
+      // IEEE division.
       const float y = __frcp_rn(sc);
       const uint64_t y2 = pack_f32x2(y, y), ns2 = pack_f32x2(-sc, -sc);
 #pragma unroll
@@ -247,21 +268,21 @@ __device__ __forceinline__ uint4 quantize16(const uint4& v0, const uint4& v1, fl
         const uint64_t x2 = pack_f32x2(f[i], f[i + 1]);
         const uint64_t q0 = mul_f32x2(x2, y2);
         const uint64_t r = fma_f32x2(ns2, q0, x2);
-        float lo, hi;
-        unpack_f32x2(fma_f32x2(r, y2, q0), lo, hi);
-        f[i] = copysignf(lo, f[i]);
-        f[i + 1] = copysignf(hi, f[i + 1]);
+        unpack_f32x2(fma_f32x2(r, y2, q0), f[i], f[i + 1]);
       }
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], sc);
     }
   }
+  // Each code takes its input's sign bit: it changes only the +0 that the
+  // correction step makes of -0 / s (a quotient's sign is x's otherwise, and
+  // the codes of s = 0 are x's own).
   uint4 q;
-  q.x = e4m3x4(f[0], f[1], f[2], f[3]);
-  q.y = e4m3x4(f[4], f[5], f[6], f[7]);
-  q.z = e4m3x4(f[8], f[9], f[10], f[11]);
-  q.w = e4m3x4(f[12], f[13], f[14], f[15]);
+  q.x = e4m3x4(f[0], f[1], f[2], f[3]) | bf16_signs4(v0.x, v0.y);
+  q.y = e4m3x4(f[4], f[5], f[6], f[7]) | bf16_signs4(v0.z, v0.w);
+  q.z = e4m3x4(f[8], f[9], f[10], f[11]) | bf16_signs4(v1.x, v1.y);
+  q.w = e4m3x4(f[12], f[13], f[14], f[15]) | bf16_signs4(v1.z, v1.w);
   return q;
 }
 
