@@ -183,7 +183,7 @@ cudaError_t launch_kernel(void (*fn)(Params...), dim3 grid, dim3 block, size_t s
 // counts arrivals and is zero between launches, bar[1] is a generation
 // number. Thread 0 of every block reads the generation early in the launch
 // (barrier_generation), before it can change; the last block to arrive
-// clears the count and then bumps the generation, which releases the others.
+// bumps the generation, which releases the others, and then clears the count.
 // So a workspace that was zero-filled once needs no reset between calls. A
 // block whose arrival count comes back >= nblocks found leftover words (a
 // workspace never zero-filled, or one an aborted launch left behind): it
@@ -207,9 +207,12 @@ __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, un
     if (old >= nblocks) {
       flag(status, EP_ST_WORKSPACE);
     } else if (old == nblocks - 1) {
-      atomicExch(&bar[0], 0u);
       __threadfence();
       atomicAdd(&bar[1], 1u);
+      // Every block has arrived, none reads the count again in this launch,
+      // and the next launch starts after this one completes: the reset is a
+      // plain store after the release, off the others' critical path.
+      *reinterpret_cast<volatile unsigned*>(&bar[0]) = 0u;
     } else {
       const unsigned long long t0 = global_ns();
       while (ld_acquire_u32(bar + 1) == gen0) {
@@ -220,7 +223,8 @@ __device__ __forceinline__ void grid_barrier(unsigned* bar, unsigned nblocks, un
         __nanosleep(32);
       }
     }
-    __threadfence();
+    // (The acquire load that saw the new generation orders this block's
+    // later reads; they read the chunk counts from L2.)
   }
   __syncthreads();
 }

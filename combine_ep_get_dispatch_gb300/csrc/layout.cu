@@ -15,19 +15,23 @@
 // coding each entry as (expert, rank, first-slot-of-the-token-on-that-rank;
 // the flag from the token's earlier slots, neighbours of the entry's own
 // index); divisions by E/R and K are multiply-highs. Pass 1 counts per warp with
-// shared-memory atomics. A shuffle scan across warps gives each warp its
-// prefix; the chunk totals go to global memory; one bounded grid barrier
-// (cooperative launch); every CTA then sums the chunk totals before it (its
-// prefix) and all of them (the totals) and scans the totals over experts and
-// ranks in one pass. Pass 2 walks the warp's range 32 entries at a time: ballots on the
-// key bits give each lane the lanes with the same expert (rank), so its
-// position among them is a popcount and one leader bumps the warp's counter.
-// No atomics decide an order: slots follow (token, slot) order by
-// construction. The kernel is bound by instruction latency, not memory: the
-// traffic is a few hundred KB of int32.
+// shared-memory atomics. One thread per column then walks the warps' counts,
+// leaving each warp its prefix (a shuffle scan per column across the warps
+// was bound by shuffle throughput: 2.2 of the kernel's 13.3 us at 16384
+// tokens, against 0.6 us for the walk); the chunk totals go to global
+// memory; one bounded grid barrier (cooperative launch); every CTA then sums
+// the chunk totals before it (its prefix) and all of them (the totals), and
+// warp 0 scans the totals over experts and ranks in one pass. Pass 2 walks the
+// warp's range 32 entries at a time: ballots on the key bits give each lane
+// the lanes with the same expert (rank); its slot is the warp's running count
+// plus the chunk prefix and the global offset plus its position among them (a
+// popcount), and one leader bumps the warp's counter. No atomics decide an
+// order: slots follow (token, slot) order by construction. The kernel is
+// bound by instruction latency, not memory: the traffic is a few hundred KB
+// of int32.
 // Low latency: chunks are source ranks. A small batch instead runs as one CTA
-// in which a group of g warps holds each source rank's entries: the scan
-// across warps then gives the prefix over source ranks, and no grid barrier
+// in which a group of g warps holds each source rank's entries: the walk
+// over the warps then gives the prefix over source ranks, and no grid barrier
 // or exchange through memory is needed (nor with a single chunk in normal
 // mode).
 #include "common.cuh"
@@ -37,41 +41,32 @@ namespace ep {
 
 constexpr int kMaxLayoutThreads = 1024;
 
-// Exclusive scan of a[0..n) in shared memory, in place; returns the total.
-// All threads of the block must call it; warp_tmp holds 32 ints.
-__device__ int block_exclusive_scan(int32_t* a, int n, int32_t* warp_tmp) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nthreads = blockDim.x, nwarps = nthreads >> 5;
-  const int per = (n + nthreads - 1) / nthreads;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int s = 0;
-  for (int i = lo; i < hi; ++i) s += a[i];
-  int v = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
-  }
-  if (lane == 31) warp_tmp[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int x = lane < nwarps ? warp_tmp[lane] : 0;
+// Exclusive scan of a[0..n) in shared memory by warp 0 (lane l scans a run
+// of ceil(n / 32) entries, a shuffle scan joins the runs); returns the total
+// to every thread. a[] must be complete; all threads must call it.
+__device__ int warp0_exclusive_scan(int32_t* a, int n, int32_t* tmp) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    int s = 0;
+    for (int i = lo; i < hi; ++i) s += a[i];
+    int v = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
     }
-    if (lane < nwarps) warp_tmp[lane] = x;
+    int run = v - s;
+    for (int i = lo; i < hi; ++i) {
+      const int x = a[i];
+      a[i] = run;
+      run += x;
+    }
+    if (lane == 31) tmp[0] = v;
   }
   __syncthreads();
-  int run = (w > 0 ? warp_tmp[w - 1] : 0) + v - s;
-  const int total = warp_tmp[nwarps - 1];
-  for (int i = lo; i < hi; ++i) {
-    const int x = a[i];
-    a[i] = run;
-    run += x;
-  }
-  __syncthreads();
-  return total;
+  return tmp[0];
 }
 
 // Entry code of one (token, slot): -1 for "no expert" (masked, or an index
@@ -218,46 +213,35 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
   if (__any_sync(0xffffffffu, bad) && lane == 0) flag(p.status, EP_ST_BAD_INDEX);
   __syncthreads();
 
-  // Per column: exclusive prefix over warps (one warp per column, lane = warp
-  // index, shuffle scan); the chunk's total goes out. A warp takes its
-  // columns kScanCols at a time, their shuffle chains interleaved.
-  constexpr int kScanCols = 8;
-  for (int c0 = w; c0 < C; c0 += W * kScanCols) {
-    int v[kScanCols], incl[kScanCols];
+  // Per column: exclusive prefix over warps, one thread per column walking
+  // the warps' counts (consecutive threads, consecutive columns: no bank
+  // conflict; eight loads in flight at a time); the chunk's total goes out.
+  for (int col = tid; col < C; col += NT) {
+    const bool ranges = warp_src && col < E;
+    const int g = ranges ? p.ll_src_warps : 1;
+    int run = 0, lo = 0;
+    for (int w0 = 0; w0 < W; w0 += 8) {
+      int x[8];
 #pragma unroll
-    for (int j = 0; j < kScanCols; ++j) {
-      const int col = c0 + j * W;
-      v[j] = (lane < W && col < C) ? hist[lane * CP + col] : 0;
-      incl[j] = v[j];
-    }
+      for (int u = 0; u < 8; ++u) x[u] = (w0 + u < W) ? hist[(w0 + u) * CP + col] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-      for (int j = 0; j < kScanCols; ++j) {
-        const int y = __shfl_up_sync(0xffffffffu, incl[j], o);
-        if (lane >= o) incl[j] += y;
+      for (int u = 0; u < 8; ++u) {
+        const int w2 = w0 + u;
+        if (w2 < W) hist[w2 * CP + col] = run;
+        if (ranges && w2 < W && w2 % g == 0) lo = run;
+        run += x[u];
+        if (ranges && w2 < W && w2 % g == g - 1) {
+          // One-CTA low-latency form: warps [s*g, (s+1)*g) hold source rank
+          // s, so its range of expert col is (prefix before its first warp,
+          // count up to the end of its last warp).
+          const int64_t l = min(static_cast<int64_t>(lo), p.ll_cap);
+          const int64_t h = min(static_cast<int64_t>(run), p.ll_cap);
+          p.ll_range[static_cast<int64_t>(col) * R + w2 / g] = (l << 32) | (h - l);
+        }
       }
     }
-#pragma unroll
-    for (int j = 0; j < kScanCols; ++j) {
-      const int col = c0 + j * W;
-      if (col >= C) break;
-      if (warp_src && col < E) {
-        // One-CTA low-latency form: warps [s*g, (s+1)*g) hold source rank s,
-        // so its range of expert col is (prefix before its first warp, count
-        // up to the end of its last warp).
-        const int g = p.ll_src_warps;
-        const int last = __shfl_sync(0xffffffffu, incl[j], min(lane + g - 1, 31));
-        const int64_t lo = min(static_cast<int64_t>(incl[j] - v[j]), p.ll_cap);
-        const int64_t hi = min(static_cast<int64_t>(last), p.ll_cap);
-        if (lane < W && lane % g == 0) p.ll_range[static_cast<int64_t>(col) * R + lane / g] = (lo << 32) | (hi - lo);
-      }
-      if (lane < W) hist[lane * CP + col] = incl[j] - v[j];
-      if (lane == 31) {
-        own[col] = incl[j];
-        if (G > 1) p.ws_chunk[static_cast<int64_t>(cta) * C + col] = incl[j];
-      }
-    }
+    own[col] = run;
+    if (G > 1) p.ws_chunk[static_cast<int64_t>(cta) * C + col] = run;
   }
   if (G > 1)
     grid_barrier(p.ws_barrier, static_cast<unsigned>(G), gen0, p.status);
@@ -273,84 +257,124 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     }
   }
 
-  // Prefix over earlier chunks and totals over all chunks. P threads share a
-  // column (four columns when C % 4 == 0: 16-byte loads), each summing every
-  // P-th chunk with all of its loads in flight at once.
-  // One CTA: no other chunks, the totals are its own counts.
+  // Prefix over earlier chunks and totals over all chunks (four columns per
+  // 16-byte load when C % 4 == 0). One CTA: no other chunks, the totals are
+  // its own counts.
   const int CV = (C % 4 == 0) ? C / 4 : 0;   // 16-byte column groups
   const int P = CV ? max(1, min(NT / CV, G)) : max(1, min(NT / C, G));
-  if (G > 1 && CV) {
-    const int4* chunk4 = reinterpret_cast<const int4*>(p.ws_chunk);
-    for (int j = tid; j < P * CV; j += NT) {
-      const int cv = j % CV, pp = j / CV;
-      int4 pre = make_int4(0, 0, 0, 0), total = pre;
-      for (int c = pp; c < G; c += 8 * P) {
-        int4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = (c + u * P < G) ? __ldcg(chunk4 + static_cast<int64_t>(c + u * P) * CV + cv) : make_int4(0, 0, 0, 0);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const bool before = c + u * P < cta;
-          pre.x += before ? v[u].x : 0; pre.y += before ? v[u].y : 0;
-          pre.z += before ? v[u].z : 0; pre.w += before ? v[u].w : 0;
-          total.x += v[u].x; total.y += v[u].y; total.z += v[u].z; total.w += v[u].w;
-        }
-      }
-      const int col = 4 * cv;  // part[pp * C + col .. col + 3]
-      part[pp * C + col] = pre.x; part[pp * C + col + 1] = pre.y;
-      part[pp * C + col + 2] = pre.z; part[pp * C + col + 3] = pre.w;
-      part[PS + pp * C + col] = total.x; part[PS + pp * C + col + 1] = total.y;
-      part[PS + pp * C + col + 2] = total.z; part[PS + pp * C + col + 3] = total.w;
-    }
-  }
-  for (int j = tid; G > 1 && !CV && j < P * C; j += NT) {
-    const int col = j % C, pp = j / C;
-    int pre = 0, total = 0, c = pp;
-    for (; c + 7 * P < G; c += 8 * P) {
-      int v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(p.ws_chunk + static_cast<int64_t>(c + u * P) * C + col);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        pre += (c + u * P < cta) ? v[u] : 0;
-        total += v[u];
-      }
-    }
-    for (; c < G; c += P) {
-      const int v = __ldcg(p.ws_chunk + static_cast<int64_t>(c) * C + col);
-      pre += (c < cta) ? v : 0;
-      total += v;
-    }
-    part[j] = pre;  // j < P * C <= PS
-    part[PS + j] = total;
-  }
-  if (G > 1) __syncthreads();
-  for (int col = tid; col < C; col += NT) {
-    int pre = 0, total = own[col];
-    if (G > 1) {
-      total = 0;
-      for (int pp = 0; pp < P; ++pp) {
-        pre += part[pp * C + col];
-        total += part[PS + pp * C + col];
-      }
-    }
+  // Column totals and this chunk's prefix land in tot[] / base[]; cta 0 also
+  // writes the counts. Aligned layouts scan the padded segment lengths (the
+  // counts stay true).
+  auto put = [&](int col, int pre, int total) {
     base[col] = pre;
-    tot[col] = total;
     if (cta == 0) {
       if (col < E)
         p.per_expert[col] = total;
       else
         p.per_rank[col - E] = total;
     }
+    if (p.align > 1 && col < E) total = (total + p.align - 1) / p.align * p.align;
+    tot[col] = total;
+  };
+  // Up to 64 chunks: an octet of lanes per group of four columns, each lane
+  // summing every eighth chunk (at most eight loads, all in flight at once);
+  // shuffles reduce the octet. More chunks: P threads per column group, each
+  // summing every P-th chunk, partial sums reduced through shared memory.
+  constexpr int kOct = 8;
+  if (G > 1 && CV && CV * kOct <= NT && G <= 8 * kOct) {
+    const int4* chunk4 = reinterpret_cast<const int4*>(p.ws_chunk);
+    const bool act = tid < CV * kOct;  // whole octets: CV * kOct is a multiple of 8
+    const int cv = tid / kOct, pp = tid % kOct;
+    int4 pre = make_int4(0, 0, 0, 0), total = pre;
+    if (act) {
+      int4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = (pp + u * kOct < G) ? __ldcg(chunk4 + static_cast<int64_t>(pp + u * kOct) * CV + cv)
+                                   : make_int4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool before = pp + u * kOct < cta;
+        pre.x += before ? v[u].x : 0; pre.y += before ? v[u].y : 0;
+        pre.z += before ? v[u].z : 0; pre.w += before ? v[u].w : 0;
+        total.x += v[u].x; total.y += v[u].y; total.z += v[u].z; total.w += v[u].w;
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < kOct; o <<= 1) {
+      pre.x += __shfl_xor_sync(0xffffffffu, pre.x, o); pre.y += __shfl_xor_sync(0xffffffffu, pre.y, o);
+      pre.z += __shfl_xor_sync(0xffffffffu, pre.z, o); pre.w += __shfl_xor_sync(0xffffffffu, pre.w, o);
+      total.x += __shfl_xor_sync(0xffffffffu, total.x, o); total.y += __shfl_xor_sync(0xffffffffu, total.y, o);
+      total.z += __shfl_xor_sync(0xffffffffu, total.z, o); total.w += __shfl_xor_sync(0xffffffffu, total.w, o);
+    }
+    if (act && pp == 0) {
+      put(4 * cv, pre.x, total.x); put(4 * cv + 1, pre.y, total.y);
+      put(4 * cv + 2, pre.z, total.z); put(4 * cv + 3, pre.w, total.w);
+    }
+  } else {
+    if (G > 1 && CV) {
+      const int4* chunk4 = reinterpret_cast<const int4*>(p.ws_chunk);
+      for (int j = tid; j < P * CV; j += NT) {
+        const int cv = j % CV, pp = j / CV;
+        int4 pre = make_int4(0, 0, 0, 0), total = pre;
+        for (int c = pp; c < G; c += 8 * P) {
+          int4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            v[u] = (c + u * P < G) ? __ldcg(chunk4 + static_cast<int64_t>(c + u * P) * CV + cv) : make_int4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const bool before = c + u * P < cta;
+            pre.x += before ? v[u].x : 0; pre.y += before ? v[u].y : 0;
+            pre.z += before ? v[u].z : 0; pre.w += before ? v[u].w : 0;
+            total.x += v[u].x; total.y += v[u].y; total.z += v[u].z; total.w += v[u].w;
+          }
+        }
+        const int col = 4 * cv;  // part[pp * C + col .. col + 3]
+        part[pp * C + col] = pre.x; part[pp * C + col + 1] = pre.y;
+        part[pp * C + col + 2] = pre.z; part[pp * C + col + 3] = pre.w;
+        part[PS + pp * C + col] = total.x; part[PS + pp * C + col + 1] = total.y;
+        part[PS + pp * C + col + 2] = total.z; part[PS + pp * C + col + 3] = total.w;
+      }
+    }
+    for (int j = tid; G > 1 && !CV && j < P * C; j += NT) {
+      const int col = j % C, pp = j / C;
+      int pre = 0, total = 0, c = pp;
+      for (; c + 7 * P < G; c += 8 * P) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(p.ws_chunk + static_cast<int64_t>(c + u * P) * C + col);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          pre += (c + u * P < cta) ? v[u] : 0;
+          total += v[u];
+        }
+      }
+      for (; c < G; c += P) {
+        const int v = __ldcg(p.ws_chunk + static_cast<int64_t>(c) * C + col);
+        pre += (c < cta) ? v : 0;
+        total += v;
+      }
+      part[j] = pre;  // j < P * C <= PS
+      part[PS + j] = total;
+    }
+    if (G > 1) __syncthreads();
+    for (int col = tid; col < C; col += NT) {
+      int pre = 0, total = own[col];
+      if (G > 1) {
+        total = 0;
+        for (int pp = 0; pp < P; ++pp) {
+          pre += part[pp * C + col];
+          total += part[PS + pp * C + col];
+        }
+      }
+      put(col, pre, total);
+    }
   }
-  // Aligned layouts scan the padded segment lengths (the counts stay true).
-  if (p.align > 1)
-    for (int e = tid; e < E; e += NT) tot[e] = (tot[e] + p.align - 1) / p.align * p.align;
   __syncthreads();
-  // One scan over the expert and the rank columns together; a rank column's
-  // offset is its prefix minus the expert total.
-  const int total_c = block_exclusive_scan(tot, C, tmp);
+  // One scan over the expert and the rank columns together (by warp 0); a
+  // rank column's offset is its prefix minus the expert total.
+  const int total_c = warp0_exclusive_scan(tot, C, tmp);
   const int total_e = kRank ? tot[E] : total_c;
   const int total_r = total_c - total_e;
   if (cta == 0 && !kLL) {
@@ -370,11 +394,6 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     }
     if (cta == 0 && tid == 0) *p.ll_hdr = p.hdr_value;
   }
-  // Running counters: warp prefix + chunk prefix (+ global offset in normal mode).
-  for (int col = w; col < C; col += W) {
-    if (lane < W) hist[lane * CP + col] += base[col] + (kLL ? 0 : tot[col] - (col >= E ? total_e : 0));
-  }
-  __syncthreads();
 
   // Pass 2: slots, in (token, slot) order within the warp's range.
   bool overflow = false, bad2 = false;
@@ -386,14 +405,15 @@ __global__ void __launch_bounds__(kMaxLayoutThreads) layout_kernel(const LayoutP
     const bool valid = code >= 0;
     const int e = code_e(code);
     const unsigned pe = warp_peers(e, valid, p.bits_E);
-    const int slot = valid ? my[e] + __popc(pe & lanemask_lt()) : -1;
+    // warp prefix (running) + chunk prefix (+ global offset in normal mode)
+    const int slot = valid ? my[e] + base[e] + (kLL ? 0 : tot[e]) + __popc(pe & lanemask_lt()) : -1;
     const bool first = kRank && valid && (code & kFirstBit);
     const int r = code_r(code);
     unsigned pr = 0;
     int rslot = -1;
     if (kRank) {
       pr = warp_peers(r, first, p.bits_R);
-      rslot = first ? my[E + r] + __popc(pr & lanemask_lt()) : -1;
+      rslot = first ? my[E + r] + base[E + r] + (kLL ? 0 : tot[E + r] - total_e) + __popc(pr & lanemask_lt()) : -1;
     }
     __syncwarp();
     if (valid && lane == __ffs(pe) - 1) my[e] += __popc(pe);
