@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) dispatch_bf16_kernel(const Dis
 // dispatches from 90.1 to 86.0 us and 79.9 to 74.2 us).
 constexpr int kF8Warps = 4;                  // warps per token (one token per block)
 constexpr size_t kF8StagedBytesPerSM = 105 * 1024;  // see launch_fp8
+constexpr size_t kF8MaxBlocksPerSM = 10;
 constexpr size_t kSmemPerSM = 228 * 1024;            // shared memory of one SM
 constexpr size_t kSmemReservedPerBlock = 1024;       // the runtime's share of it per block
 constexpr int kF8MaxDest = 2 * EP_MAX_TOPK;  // <= K expert copies + <= K rank copies
@@ -864,12 +865,16 @@ cudaError_t launch_ex(void (*fn)(Params), unsigned grid, unsigned threads, size_
 // to the freed slots.
 cudaError_t launch_fp8(const DispatchParams& p, cudaStream_t s, bool pdl) {
   if (p.N <= 0) return cudaSuccess;
-  // At most kF8StagedBytesPerSM of staged rows per SM: every block of the
-  // first wave loads its row at once, so this caps the first wave's read
-  // burst (and its synchronous quantisation) before the first stores; the
-  // request for more shared memory than a block needs is what caps it.
+  // At most kF8StagedBytesPerSM of staged rows, and kF8MaxBlocksPerSM
+  // blocks, per SM: every block of the first wave loads its row at once, so
+  // this caps the first wave's read burst (and its synchronous quantisation)
+  // before the first stores; the request for more shared memory than a
+  // block needs is what caps it. Measured on GB300 (4096 tokens at hidden
+  // 7168: 6 / 7 / 8 blocks 79.8 / 77.8 / 81.1 us; 8192 tokens at hidden
+  // 4096: 9 / 10 / 11 / 12 blocks 71.3 / 70.6 / 70.9 / 71.5 us).
   size_t smem = kBarBytes + f8_warp_bytes(p.H);
-  const size_t blocks = kF8StagedBytesPerSM / smem;
+  size_t blocks = kF8StagedBytesPerSM / smem;
+  if (blocks > kF8MaxBlocksPerSM) blocks = kF8MaxBlocksPerSM;
   if (blocks >= 1 && blocks < kSmemPerSM / (smem + kSmemReservedPerBlock)) {
     const size_t capped = kSmemPerSM / blocks - kSmemReservedPerBlock - 256;
     if (capped > smem) smem = capped;
